@@ -1,0 +1,200 @@
+/*
+ * rapid.h - C ABI of librapid.so: the long-context verification step of
+ * retrieval-augmented speculative decoding on one GB300 (sm_103a).
+ *
+ * Two operations make up the step:
+ *
+ *   rapid_verify_attn  attention of the n_q = gamma+1 draft/query tokens of a
+ *                      verify pass against a long GQA KV cache, computed as
+ *                      "hybrid tree attention": an unmasked pass over the
+ *                      history (prefix) rows, a masked pass over the n_q
+ *                      speculative rows, and an exact log-sum-exp merge of the
+ *                      two partial results.
+ *                      Source: "LongSpec: Long-Context Lossless Speculative
+ *                      Decoding with Efficient Drafting and Verification",
+ *                      section 2.3 (Fast Tree Attention / Hybrid Tree
+ *                      Attention): history part without a mask, speculative
+ *                      part with a mask, parts combined by log-sum-exp.
+ *
+ *   rapid_accept       the retrieval-augmented acceptance step over the full
+ *                      vocabulary.  Source: "RAPID: Long-Context Inference
+ *                      with Retrieval-Augmented Speculative Decoding" (blog
+ *                      summary), section 2.1 (speculative-decoding ratio test
+ *                      and residual distribution) and section 2.4 (the
+ *                      retrieval-augmented target p_hat = softmax(z/T +
+ *                      eta*(q - p)), the tail-preserving replacement of p_hat
+ *                      by p where p_hat < 0.1 * max p_hat, and the adjusted
+ *                      residual norm(max(p - p_hat, p - q))).
+ *
+ * Conventions shared by every call:
+ *  - All tensor arguments are DEVICE pointers owned by the caller.  The library
+ *    allocates nothing on these paths; scratch space is the caller's
+ *    `workspace` (size from the matching *_workspace_size call, 256-byte
+ *    aligned).  The library never writes to the KV cache.
+ *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t
+ *    passed as void*; NULL = the legacy default stream).  No call
+ *    synchronises the device; results are valid once the stream reaches them.
+ *  - Argument checks that need only host-visible values run before any launch
+ *    and return RAPID_EINVAL.  Values that live in device memory (prefix
+ *    lengths, masks, token ids, parent pointers) are clamped by the kernels to
+ *    keep every memory access in bounds; an out-of-range device value gives
+ *    unspecified (but memory-safe) results.
+ *  - No C++ exception crosses this ABI.  Calls are stateless and may be issued
+ *    from several host threads on different streams.
+ */
+#ifndef RAPID_H
+#define RAPID_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RAPID_OK = 0,
+    RAPID_EINVAL = -1,      /* bad argument (host-checkable)                 */
+    RAPID_ECUDA = -2,       /* a CUDA runtime call or kernel launch failed   */
+    RAPID_ENOMEM = -3,      /* workspace smaller than the *_workspace_size   */
+    RAPID_EUNSUPPORTED = -4 /* shape outside the compiled kernels' limits    */
+} rapid_status;
+
+/* Element types of Q, K, V and O. */
+enum { RAPID_DTYPE_F32 = 0, RAPID_DTYPE_BF16 = 1 };
+
+/* Flags of rapid_accept. */
+enum {
+    /* Keep p where p_hat < 0.1 * max(p_hat) ("retrieval-augmented target
+     * distribution" section: the tail of p_hat is replaced by the tail of p).
+     * Set by default in the Python binding; clear it for the plain p_hat. */
+    RAPID_ACCEPT_TAIL_CLAMP = 1u
+};
+
+/* Largest sizes the compiled kernels accept. */
+enum {
+    RAPID_MAX_NQ = 64,        /* query (draft) tokens per sequence            */
+    RAPID_MAX_VOCAB = 262144  /* vocabulary entries per row                   */
+};
+
+/* ------------------------------------------------------------------------ */
+/* Verify attention                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of scratch that rapid_verify_attn needs for these sizes.  Returns 0
+ * for sizes that rapid_verify_attn would reject.
+ */
+size_t rapid_verify_attn_workspace_size(int B, int Hq, int Hkv, int d, int n_q,
+                                        int64_t kv_capacity, int dtype);
+
+/*
+ * O, LSE = attention of the verify queries against the KV cache.
+ *
+ *  Q          [B, Hq, n_q, d]          dtype; already rotated (RoPE applied).
+ *  Kcache     [B, Hkv, kv_capacity, d] dtype; key rows, head-major.
+ *  Vcache     [B, Hkv, kv_capacity, d] dtype; value rows, head-major.
+ *  dtype      RAPID_DTYPE_BF16 or RAPID_DTYPE_F32 (all of Q, K, V, O).
+ *  d          head dimension: 64 or 128.
+ *  n_q        query tokens per sequence, 1..RAPID_MAX_NQ.  Query head h uses
+ *             KV head h / (Hq / Hkv) (grouped-query attention).
+ *  prefix_len device int32 [B]: history rows of sequence b are
+ *             [0, prefix_len[b]); its n_q speculative rows are
+ *             [prefix_len[b], prefix_len[b] + n_q).  Needs
+ *             0 <= prefix_len[b] <= kv_capacity - n_q.
+ *  spec_mask  device uint8 [B, n_q, n_q] or NULL.  Query i of sequence b sees
+ *             speculative row j iff spec_mask[b][i][j] != 0 (a token tree's
+ *             ancestor-or-self mask).  NULL means the causal chain j <= i.
+ *             Every history row is visible to every query (no mask there).
+ *  softmax_scale  score multiplier; <= 0 selects 1/sqrt(d).
+ *  O          [B, Hq, n_q, d] dtype: softmax-weighted sum of the visible V rows.
+ *  LSE        float [B, Hq, n_q]: natural-log log-sum-exp of the scaled scores
+ *             over the visible rows.
+ *  workspace  device scratch of at least rapid_verify_attn_workspace_size()
+ *             bytes, 256-byte aligned; contents need no initialisation.
+ *
+ * Errors: RAPID_EINVAL for NULL tensors, d not in {64,128}, Hq % Hkv != 0,
+ * n_q outside [1, RAPID_MAX_NQ], B < 1, kv_capacity < n_q, misaligned
+ * pointers (16 bytes); RAPID_ENOMEM for a short workspace; RAPID_ECUDA when a
+ * launch fails.
+ */
+rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vcache,
+                               int dtype, int B, int Hq, int Hkv, int d, int n_q,
+                               int64_t kv_capacity, const int32_t* prefix_len,
+                               const uint8_t* spec_mask, float softmax_scale,
+                               void* O, float* LSE, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Acceptance                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of scratch that rapid_accept needs; 0 for rejected sizes. */
+size_t rapid_accept_workspace_size(int B, int n_q, int V);
+
+/*
+ * Retrieval-augmented acceptance of one verify step.
+ *
+ *  z_target     device float [B, n_q, V]: target logits.  Row j of sequence b
+ *               is the target's next-token distribution after node j (node 0
+ *               is the last committed token, nodes 1..n_q-1 are drafts).
+ *  q_draft      device float [B, n_q, V]: draft probabilities for the same
+ *               rows (rows sum to 1; taken as given, T does not touch them).
+ *  draft_tokens device int32 [B, n_q]: token of node i (entry 0 unused).
+ *  parent       device int32 [B, n_q] or NULL.  NULL = chain (parent of node
+ *               i is i-1).  Otherwise parent[b][i] in [0, i) for i >= 1 gives
+ *               a token tree; entry 0 is unused.
+ *  T            temperature > 0; eta >= 0 and finite (knowledge-transfer
+ *               strength of the retrieval-augmented target).
+ *  philox_seed  key of the Philox4x32-10 stream.  Node i of sequence b uses
+ *               block (counter = {i, b, 0, 0}, key = {seed & 0xffffffff,
+ *               seed >> 32}); word 0 gives r_i (ratio test of node i), word 1
+ *               gives u_i.  A uniform is (word >> 8) * 2^-24.
+ *  flags        RAPID_ACCEPT_TAIL_CLAMP or 0.
+ *
+ * Per row j:  p = softmax(z_j / T);  p_hat = softmax(z_j / T + eta (q_j - p));
+ * with the tail clamp, p_hat_k := p_k wherever p_hat_k < 0.1 * max p_hat.
+ * Node i >= 1 is accepted iff r_i <= min(1, p_hat_j(t_i) / q_j(t_i)) with
+ * j = parent(i) (q_j(t_i) = 0 accepts).  For a chain, acceptance stops at the
+ * first rejected node; for a tree, every root-to-leaf path is checked the same
+ * way and the path with the most accepted nodes wins (ties: smallest leaf
+ * index).  Let e be the last accepted node of the winning path (0 if none).
+ * The next token is drawn from row e by inverse CDF in token-id order with
+ * uniform u_{e+1}: from norm(max(p - p_hat, p - q, 0)) if node e has children
+ * (a rejection happened below it; p itself if that residual has zero mass),
+ * else from p (the bonus token after a fully accepted path).
+ *
+ * Outputs (device):  n_accepted int32 [B] (accepted draft nodes, 0..depth),
+ * next_token int32 [B], path int32 [B, n_q] or NULL (node ids of the
+ * accepted nodes in root-to-leaf order, then -1), diag float [B, n_q, 5] or
+ * NULL (for node i >= 1: p_j(t_i), clamped p_hat_j(t_i), q_j(t_i), ratio, r_i;
+ * node 0 gets zeros).
+ *
+ * Errors: RAPID_EINVAL for NULL required tensors, B < 1, n_q outside
+ * [1, RAPID_MAX_NQ], V outside [1, RAPID_MAX_VOCAB], T <= 0 or not finite,
+ * eta < 0 or not finite; RAPID_ENOMEM for a short workspace; RAPID_ECUDA when
+ * a launch fails.
+ */
+rapid_status rapid_accept(const float* z_target, const float* q_draft,
+                          const int32_t* draft_tokens, const int32_t* parent,
+                          int B, int n_q, int V, float T, float eta,
+                          uint64_t philox_seed, uint32_t flags,
+                          int32_t* n_accepted, int32_t* next_token, int32_t* path,
+                          float* diag, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Misc                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Static, NUL-terminated description of a status code. */
+const char* rapid_status_string(int status);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int rapid_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAPID_H */
