@@ -1,0 +1,395 @@
+"""Benchmark of the verification step (verify attention over every layer + acceptance).
+
+Default workload: Llama-3.1-8B-shaped, 32 layers of 32 query / 8 KV heads,
+head_dim 128, bf16 KV cache of 122880 history tokens per layer (16.1 GB, read
+once per step: larger than L2, so no flush is needed), gamma = 10 chain
+(11 query tokens), acceptance over vocab 128256 with T = 1, eta = 1.
+
+One JSON line on stdout (rank 0).  `value` = verify steps/s with all inputs
+resident in HBM; `e2e` = the same through the public API with the per-step
+inputs copied from pinned host memory and the results copied back inside the
+timed region.  `--impl reference` times the double-precision CPU oracle on a
+bounded sample of the same workload instead (it is the reference arm here).
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-step KV-cache HBM GB/s vs GB300 peak; verify steps/s at 120K context"
+UNIT = "verify_steps/s"
+WORKLOAD = "llama3.1-8b_32layers_120k"
+SRC_FILES_TRAFFIC = ["long_context_speculative_gb300/csrc/attn_tc.cu",
+                     "long_context_speculative_gb300/csrc/attn_simt.cu"]
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _traffic_for(kernel_key: str):
+    """ncu DRAM bytes per launch from profiles/traffic.json, if the kernel source
+    is unchanged since the capture (sha256 of its sources), else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            tr = json.load(f)
+        ent = tr[kernel_key]
+        h = hashlib.sha256()
+        for p in SRC_FILES_TRAFFIC:
+            with open(os.path.join(ROOT, p), "rb") as f:
+                h.update(f.read())
+        if ent.get("src_sha256") != h.hexdigest():
+            return None
+        return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def src_hash():
+    h = hashlib.sha256()
+    for p in SRC_FILES_TRAFFIC:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline of our arm, and the whole reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_time(w, layers_sample=1, groups_sample=1, seed=0):
+    """Seconds per verify step of the oracle, from a bounded sample: the
+    attention of `groups_sample` KV-head groups of `layers_sample` layers plus
+    the full acceptance, scaled to all groups and layers."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from long_context_speculative_gb300 import workloads as wl
+
+    cores = oracle.default_threads()
+    t_attn = 0.0
+    rows_done = 0
+    for layer in range(layers_sample):
+        g = torch.Generator().manual_seed(seed + layer)
+        G = w.G
+        cap = w.capacity
+        K = torch.randn((1, 1, cap, w.d), generator=g).to(torch.bfloat16)
+        V = torch.randn((1, 1, cap, w.d), generator=g).to(torch.bfloat16)
+        Q = torch.randn((1, G, w.n_q, w.d), generator=g).to(torch.bfloat16)
+        pl = np.array([w.prefix], np.int32)
+        for _ in range(groups_sample):
+            t0 = time.perf_counter()
+            oracle.verify_attn(wl.bf16_bits(Q), wl.bf16_bits(K), wl.bf16_bits(V), pl,
+                               dtype=oracle.DTYPE_BF16, nthreads=cores)
+            t_attn += time.perf_counter() - t0
+            rows_done += G * w.n_q
+    per_row = t_attn / rows_done
+    attn_step = per_row * w.B * w.Hq * w.n_q * w.layers
+    inp = wl.accept_inputs(w, B=1)
+    t0 = time.perf_counter()
+    oracle.accept(inp.z.numpy(), inp.q.numpy(), inp.tokens.numpy(), None, T=w.T, eta=w.eta,
+                  seed=1, nthreads=cores)
+    t_acc = time.perf_counter() - t0
+    sample = (f"{layers_sample} layer x {groups_sample} of {w.Hkv} KV-head groups "
+              f"({rows_done} query rows x {w.prefix} history rows, bf16 KV) + full acceptance "
+              f"(11 x {w.V}); scaled to {w.layers} layers x {w.Hkv} groups")
+    return attn_step + t_acc, cores, sample, t_attn + t_acc
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; warm-up steps are free
+    times = []
+    sample = ""
+    cores = 0
+    work = 0.0
+    for _ in range(args.steps):
+        t, cores, sample, wall = oracle_sample_time(w)
+        times.append(t)
+        work += wall
+    step_s = sum(times) / len(times)
+    value = 1.0 / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": w.layers, "context": w.prefix,
+                       "n_q": w.n_q, "vocab": w.V, "l2": "inputs larger than L2"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w):
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- resident inputs: one KV cache and one Q per layer ------------------
+    cap = w.capacity
+    Ks, Vs, Qs = [], [], []
+    for layer in range(w.layers):
+        a = wl.attn_inputs(w, layer=layer, device=dev)
+        Ks.append(a.K); Vs.append(a.V); Qs.append(a.Q)
+        del a
+    prefix_len = torch.full((w.B,), w.prefix, dtype=torch.int32, device=dev)
+    acc_in = wl.accept_inputs(w)
+    z = acc_in.z.to(dev); q = acc_in.q.to(dev); tok = acc_in.tokens.to(dev)
+    Os = [torch.empty_like(Qs[0]) for _ in range(w.layers)]
+    Ls = [torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
+          for _ in range(w.layers)]
+    ws_attn = torch.empty(rapid.rapid_verify_attn_workspace_size(
+        w.B, w.Hq, w.Hkv, w.d, w.n_q, cap, rapid.RAPID_DTYPE_BF16), dtype=torch.uint8, device=dev)
+    ws_acc = torch.empty(rapid.rapid_accept_workspace_size(w.B, w.n_q, w.V), dtype=torch.uint8,
+                         device=dev)
+    n_acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(w.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(seed, ev=None):
+        for layer in range(w.layers):
+            if ev is not None:
+                ev[layer].record(stream)
+            rapid.rapid_verify_attn(Qs[layer], Ks[layer], Vs[layer], prefix_len, None, 0.0,
+                                    Os[layer], Ls[layer], ws_attn)
+        if ev is not None:
+            ev[w.layers].record(stream)
+        rapid.rapid_accept(z, q, tok, None, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                           n_acc, nxt, None, None, ws_acc)
+
+    for i in range(args.warmup):
+        step(0x5EED0000 + i)
+    torch.cuda.synchronize()
+    assert rapid.rapid_device_error(True) == 0
+
+    # ---- timed region (device-resident inputs) ------------------------------
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(w.layers + 1)]
+           for _ in range(args.steps)]
+    end_ev = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            step(0x5EED0000 + s, evs[s])
+        end_ev.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    total_ms = evs[0][0].elapsed_time(end_ev)
+    attn_ms = []
+    for s in range(args.steps):
+        for layer in range(w.layers):
+            attn_ms.append(evs[s][layer].elapsed_time(evs[s][layer + 1]))
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert rapid.rapid_device_error(True) == 0
+
+    # ---- e2e through the public API with host buffers -------------------------
+    hQ = torch.empty((w.layers,) + tuple(Qs[0].shape), dtype=Qs[0].dtype).pin_memory()
+    for layer in range(w.layers):
+        hQ[layer].copy_(Qs[layer].cpu())
+    hz = acc_in.z.clone().pin_memory(); hq = acc_in.q.clone().pin_memory()
+    htok = acc_in.tokens.clone().pin_memory()
+    hO = torch.empty((w.layers,) + tuple(Os[0].shape), dtype=Os[0].dtype).pin_memory()
+    hL = torch.empty((w.layers,) + tuple(Ls[0].shape), dtype=torch.float32).pin_memory()
+    hres = torch.empty(2 * w.B, dtype=torch.int32).pin_memory()
+    dQ = torch.empty((w.layers,) + tuple(Qs[0].shape), dtype=Qs[0].dtype, device=dev)
+    h2d = hQ.numel() * hQ.element_size() + hz.numel() * 4 + hq.numel() * 4 + htok.numel() * 4
+    d2h = hO.numel() * hO.element_size() + hL.numel() * 4 + hres.numel() * 4
+    res_dev = torch.empty(2 * w.B, dtype=torch.int32, device=dev)
+
+    def e2e_step(seed):
+        dQ.copy_(hQ, non_blocking=True)
+        z.copy_(hz, non_blocking=True); q.copy_(hq, non_blocking=True)
+        tok.copy_(htok, non_blocking=True)
+        for layer in range(w.layers):
+            rapid.rapid_verify_attn(dQ[layer], Ks[layer], Vs[layer], prefix_len, None, 0.0,
+                                    Os[layer], Ls[layer], ws_attn)
+        rapid.rapid_accept(z, q, tok, None, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                           res_dev[:w.B], res_dev[w.B:], None, None, ws_acc)
+        for layer in range(w.layers):
+            hO[layer].copy_(Os[layer], non_blocking=True)
+            hL[layer].copy_(Ls[layer], non_blocking=True)
+        hres.copy_(res_dev, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for s in range(args.steps):
+        e2e_step(0x5EED0000 + s)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- numbers -----------------------------------------------------------
+    ms_per_step = total_ms / args.steps
+    value = ws * args.steps / (total_ms / 1e3)
+    e2e_value = ws * args.steps / (e2e_ms / 1e3)
+    kv_bytes = 2 * w.B * w.Hkv * (w.prefix + w.n_q) * w.d * 2
+    qo_bytes = 2 * w.B * w.Hq * w.n_q * w.d * 2 + w.B * w.Hq * w.n_q * 4
+    per_call = kv_bytes + qo_bytes
+    attn_ms.sort()
+    avg_call_ms = sum(attn_ms) / len(attn_ms)
+    achieved = per_call / (avg_call_ms * 1e-3) / 1e9
+    peak, peak_src = _peaks()
+    step_gbs = (per_call * w.layers + 2 * w.B * w.n_q * w.V * 4) / (ms_per_step * 1e-3) / 1e9
+    launches_per_step = 2 * w.layers + 2
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "layers": w.layers, "context": w.prefix,
+                       "n_q": w.n_q, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "vocab": w.V,
+                       "T": w.T, "eta": w.eta, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (16.1 GB KV per step), no flush"},
+            "kv_hbm_gbs_step": step_gbs,
+            "roofline": {"bound": "hbm", "kernel": "rapid_verify_attn (history + merge kernels)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs, copy)",
+                         "traffic": _traffic_for("verify_attn_llama8b_120k"),
+                         "algorithmic_bytes_per_launch": per_call,
+                         "avg_launch_ms": avg_call_ms},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "wall_s_timed": wall}
+    if rank == 0 and not args.no_cpu_baseline:
+        t, cores, sample, _ = oracle_sample_time(w, layers_sample=3, groups_sample=w.Hkv)
+        line["cpu_baseline"] = {"value": 1.0 / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    help="named chain workload (default: the 32-layer 120K Llama-3.1-8B step)")
+    args = ap.parse_args()
+    from long_context_speculative_gb300 import workloads as wl
+    w = wl.LLAMA8B_120K
+    if args.workload is not None:
+        w = {x.name: x for x in wl.ALL if not x.tree}[args.workload]
+    global WORKLOAD
+    WORKLOAD = w.name
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -193,6 +193,14 @@ const char* rapid_status_string(int status);
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 int rapid_version(void);
 
+/*
+ * Sticky error bits that kernels of this library raised on the CURRENT device
+ * (bit 0: a bounded wait for an asynchronous copy gave up, so the outputs of
+ * that call are invalid).  Synchronises the device to read the word; clears it
+ * when `clear` is non-zero.  Returns -1 if the word could not be read.
+ */
+int rapid_device_error(int clear);
+
 #ifdef __cplusplus
 }
 #endif

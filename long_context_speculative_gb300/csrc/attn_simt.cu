@@ -1,0 +1,293 @@
+// CUDA-core verify attention: the split-KV history kernel for every dtype and
+// head size (fp32 caches, d = 64, groups wider than the tensor-core kernel
+// takes), and the merge kernel that adds the masked speculative part and
+// combines all partials by log-sum-exp.
+//
+// Source of the decomposition: "LongSpec: Long-Context Lossless Speculative
+// Decoding with Efficient Drafting and Verification", section 2.3 (Hybrid
+// Tree Attention): unmasked attention over the history, masked attention over
+// the speculative tokens, outputs merged with the log-sum-exp trick.
+#include "attn.cuh"
+#include "common.cuh"
+
+namespace rapid {
+
+namespace {
+
+constexpr int kSimtThreads = 128;   // 4 warps
+constexpr int kSimtRows = 64;       // group rows per CTA (16 per warp)
+constexpr int kSimtRowsPerWarp = kSimtRows / 4;
+constexpr int kSimtKeys = 32;       // key rows per smem tile (one per lane)
+
+template <typename T>
+struct Vec16;  // 16-byte vector of T
+template <> struct Vec16<float> { static constexpr int N = 4; };
+template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
+
+template <typename T>
+__device__ __forceinline__ void load16_to_float(const T* src, float* dst);
+
+template <>
+__device__ __forceinline__ void load16_to_float<float>(const float* src, float* dst) {
+    float4 v = *reinterpret_cast<const float4*>(src);
+    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+}
+
+template <>
+__device__ __forceinline__ void load16_to_float<__nv_bfloat16>(const __nv_bfloat16* src, float* dst) {
+    uint4 v = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dst[2 * i] = __uint_as_float(w[i] << 16);
+        dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// One CTA = (split s, block of up to 64 group rows, sequence b * Hkv + head g).
+// Each lane owns one key of the 32-key tile for the scores and d/32 output
+// columns for the PV product; scores live in the log2 domain.
+template <typename T, int D>
+__global__ void __launch_bounds__(kSimtThreads)
+attn_prefix_simt_kernel(const AttnParams p) {
+    constexpr int DP = D + 4;                 // padded K pitch: conflict-free float4 rows
+    constexpr int NC = D / 32;                // output columns per lane
+    constexpr int VN = Vec16<T>::N;
+    extern __shared__ float4 smem_f4[];
+    float* sQ = reinterpret_cast<float*>(smem_f4);   // [64][D], pre-scaled by scale*log2e
+    float* sK = sQ + kSimtRows * D;                  // [32][DP]
+    float* sV = sK + kSimtKeys * DP;                 // [32][D]
+
+    const int s = blockIdx.x;
+    const int rb = blockIdx.y;
+    const int bg = blockIdx.z;
+    const int b = bg / p.Hkv;
+    const int g = bg % p.Hkv;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r0 = rb * kSimtRows;
+    const int nrows = min(kSimtRows, p.R - r0);
+
+    const int64_t P = clamped_prefix(p, b);
+    const int64_t lo = (int64_t)s * p.chunk;
+    const int64_t hi = (lo + p.chunk < P) ? lo + p.chunk : P;
+
+    const T* Qg = static_cast<const T*>(p.Q) + ((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q * D;
+    for (int idx = threadIdx.x; idx < kSimtRows * D; idx += kSimtThreads) {
+        const int r = idx / D;
+        const int k = idx - r * D;
+        sQ[idx] = (r < nrows) ? to_float(Qg[(int64_t)(r0 + r) * D + k]) * p.scale_log2 : 0.f;
+    }
+
+    float acc[kSimtRowsPerWarp][NC];
+    float m[kSimtRowsPerWarp], l[kSimtRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kSimtRowsPerWarp; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[i][c] = 0.f;
+    }
+
+    const T* Kh = static_cast<const T*>(p.K) + (int64_t)bg * p.cap * D;
+    const T* Vh = static_cast<const T*>(p.V) + (int64_t)bg * p.cap * D;
+
+    for (int64_t t0 = lo; t0 < hi; t0 += kSimtKeys) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < kSimtKeys * (D / VN); idx += kSimtThreads) {
+            const int key = idx / (D / VN);
+            const int k = (idx - key * (D / VN)) * VN;
+            float tk[VN], tv[VN];
+            if (t0 + key < hi) {
+                load16_to_float<T>(Kh + (t0 + key) * D + k, tk);
+                load16_to_float<T>(Vh + (t0 + key) * D + k, tv);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VN; ++e) { tk[e] = 0.f; tv[e] = 0.f; }
+            }
+#pragma unroll
+            for (int e = 0; e < VN; ++e) {
+                sK[key * DP + k + e] = tk[e];
+                sV[key * D + k + e] = tv[e];
+            }
+        }
+        __syncthreads();
+
+        const bool valid = (t0 + lane) < hi;
+        float sc[kSimtRowsPerWarp];
+#pragma unroll
+        for (int i = 0; i < kSimtRowsPerWarp; ++i) sc[i] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < D; k += 4) {
+            const float4 kv = *reinterpret_cast<const float4*>(&sK[lane * DP + k]);
+#pragma unroll
+            for (int i = 0; i < kSimtRowsPerWarp; ++i) {
+                const int r = warp + 4 * i;
+                if (r < nrows) {
+                    const float4 qv = *reinterpret_cast<const float4*>(&sQ[r * D + k]);
+                    sc[i] = fmaf(qv.x, kv.x, sc[i]);
+                    sc[i] = fmaf(qv.y, kv.y, sc[i]);
+                    sc[i] = fmaf(qv.z, kv.z, sc[i]);
+                    sc[i] = fmaf(qv.w, kv.w, sc[i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kSimtRowsPerWarp; ++i) {
+            if (warp + 4 * i >= nrows) continue;
+            const float si = valid ? sc[i] : -INFINITY;
+            const float mnew = fmaxf(m[i], warp_max(si));
+            const float corr = exp2f(m[i] - mnew);
+            const float pj = exp2f(si - mnew);
+            l[i] = l[i] * corr + warp_sum(pj);
+            m[i] = mnew;
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[i][c] *= corr;
+            sc[i] = pj;
+        }
+        const int nk = (hi - t0 < kSimtKeys) ? (int)(hi - t0) : kSimtKeys;
+        for (int j = 0; j < nk; ++j) {
+            float vv[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) vv[c] = sV[j * D + lane + 32 * c];
+#pragma unroll
+            for (int i = 0; i < kSimtRowsPerWarp; ++i) {
+                const float pj = __shfl_sync(0xffffffffu, sc[i], j);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) acc[i][c] = fmaf(pj, vv[c], acc[i][c]);
+            }
+        }
+    }
+
+    // Partial of this split: acc, (m, l).  An empty split leaves m = -inf, l = 0.
+    const int64_t slot = ((int64_t)bg * p.S + s) * p.R;
+#pragma unroll
+    for (int i = 0; i < kSimtRowsPerWarp; ++i) {
+        const int r = warp + 4 * i;
+        if (r >= nrows) continue;
+        float* dst = p.part_acc + (slot + r0 + r) * D;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) dst[lane + 32 * c] = acc[i][c];
+        if (lane == 0) {
+            p.part_ml[(slot + r0 + r) * 2 + 0] = m[i];
+            p.part_ml[(slot + r0 + r) * 2 + 1] = l[i];
+        }
+    }
+}
+
+// One warp per query row (b, h, i): masked attention over the n_q speculative
+// rows, then the log-sum-exp merge with the S history partials:
+//   M = max(m_spec, m_s);  L = sum_parts l_part 2^(m_part - M);
+//   O = sum_parts acc_part 2^(m_part - M) / L;   LSE = (M + log2 L) ln 2.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+    constexpr int NC = D / 32;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 4 + warp;
+    const int bg = blockIdx.y;
+    if (r >= p.R) return;
+    const int b = bg / p.Hkv;
+    const int g = bg % p.Hkv;
+    const int h = g * p.G + r / p.n_q;
+    const int i = r % p.n_q;
+    const int64_t P = clamped_prefix(p, b);
+
+    const T* Qrow = static_cast<const T*>(p.Q) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
+    const T* Kh = static_cast<const T*>(p.K) + (int64_t)bg * p.cap * D;
+    const T* Vh = static_cast<const T*>(p.V) + (int64_t)bg * p.cap * D;
+
+    float q[NC], acc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        q[c] = to_float(Qrow[lane + 32 * c]) * p.scale_log2;
+        acc[c] = 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < p.n_q; ++j) {
+        const bool vis = p.mask ? (p.mask[((int64_t)b * p.n_q + i) * p.n_q + j] != 0) : (j <= i);
+        if (!vis) continue;
+        const T* kr = Kh + (P + j) * D;
+        const T* vr = Vh + (P + j) * D;
+        float dot = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) dot = fmaf(q[c], to_float(kr[lane + 32 * c]), dot);
+        const float sj = warp_sum(dot);
+        const float mnew = fmaxf(m, sj);
+        const float corr = exp2f(m - mnew);
+        const float pj = exp2f(sj - mnew);
+        l = l * corr + pj;
+        m = mnew;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = fmaf(pj, to_float(vr[lane + 32 * c]), acc[c] * corr);
+    }
+
+    const float* ml = p.part_ml + ((int64_t)bg * p.S) * p.R * 2;
+    const float* pa = p.part_acc + ((int64_t)bg * p.S) * p.R * D;
+    float M = m;
+    for (int s = 0; s < p.S; ++s) {
+        const float ls = ml[((int64_t)s * p.R + r) * 2 + 1];
+        if (ls > 0.f) M = fmaxf(M, ml[((int64_t)s * p.R + r) * 2]);
+    }
+    float L = 0.f;
+    if (l > 0.f) {
+        const float w = exp2f(m - M);
+        L = l * w;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] *= w;
+    }
+    for (int s = 0; s < p.S; ++s) {
+        const float ls = ml[((int64_t)s * p.R + r) * 2 + 1];
+        if (!(ls > 0.f)) continue;
+        const float w = exp2f(ml[((int64_t)s * p.R + r) * 2] - M);
+        L = fmaf(ls, w, L);
+        const float* src = pa + ((int64_t)s * p.R + r) * D;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = fmaf(src[lane + 32 * c], w, acc[c]);
+    }
+
+    T* Orow = static_cast<T*>(p.O) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) Orow[lane + 32 * c] = from_float<T>(acc[c] * inv);
+    if (lane == 0)
+        p.LSE[((int64_t)b * p.Hq + h) * p.n_q + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+}
+
+template <typename T, int D>
+cudaError_t launch_simt_typed(const AttnParams& p, cudaStream_t st) {
+    const int smem = (kSimtRows * D + kSimtKeys * (D + 4) + kSimtKeys * D) * (int)sizeof(float);
+    auto kern = attn_prefix_simt_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.S, (p.R + kSimtRows - 1) / kSimtRows, p.B * p.Hkv);
+    kern<<<grid, kSimtThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_merge_typed(const AttnParams& p, cudaStream_t st) {
+    dim3 grid((p.R + 3) / 4, p.B * p.Hkv);
+    attn_merge_kernel<T, D><<<grid, 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_prefix_simt(const AttnParams& p, int dtype, cudaStream_t s) {
+    if (dtype == 1) {
+        return p.d == 128 ? launch_simt_typed<__nv_bfloat16, 128>(p, s)
+                          : launch_simt_typed<__nv_bfloat16, 64>(p, s);
+    }
+    return p.d == 128 ? launch_simt_typed<float, 128>(p, s) : launch_simt_typed<float, 64>(p, s);
+}
+
+cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s) {
+    if (dtype == 1) {
+        return p.d == 128 ? launch_merge_typed<__nv_bfloat16, 128>(p, s)
+                          : launch_merge_typed<__nv_bfloat16, 64>(p, s);
+    }
+    return p.d == 128 ? launch_merge_typed<float, 128>(p, s) : launch_merge_typed<float, 64>(p, s);
+}
+
+}  // namespace rapid

@@ -1,0 +1,206 @@
+// C ABI of librapid.so: argument checks, workspace planning, launches.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "accept.cuh"
+#include "attn.cuh"
+#include "common.cuh"
+#include "rapid.h"
+
+namespace rapid {
+
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+unsigned int* device_error_word() {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return static_cast<unsigned int*>(ptr);
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+struct AttnPlan {
+    bool tc;        // tensor-core history kernel
+    int S;          // splits of the history per (b, kv head)
+    int64_t chunk;  // history rows per split
+    size_t ws_bytes;
+};
+
+bool attn_args_ok(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtype) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || (Hq % Hkv) != 0) return false;
+    if (d != 64 && d != 128) return false;
+    if (n_q < 1 || n_q > RAPID_MAX_NQ) return false;
+    if (cap < n_q || cap > ((int64_t)1 << 31)) return false;
+    if (dtype != RAPID_DTYPE_F32 && dtype != RAPID_DTYPE_BF16) return false;
+    const int64_t R = (int64_t)(Hq / Hkv) * n_q;
+    if (R > 4096) return false;
+    return true;
+}
+
+AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtype) {
+    AttnPlan pl{};
+    const int G = Hq / Hkv;
+    const int R = G * n_q;
+    AttnParams probe{};
+    probe.B = B; probe.Hq = Hq; probe.Hkv = Hkv; probe.d = d; probe.n_q = n_q; probe.G = G;
+    probe.R = R; probe.cap = cap;
+    pl.tc = attn_prefix_tc_supported(probe, dtype);
+    const int64_t max_prefix = cap - n_q;
+    const int sms = sm_count();
+    int64_t chunk;
+    if (pl.tc) {
+        // One CTA per SM: spread B * Hkv heads over all SMs.
+        const int64_t heads = (int64_t)B * Hkv;
+        int64_t S = (sms + heads - 1) / heads;
+        if (S < 1) S = 1;
+        chunk = (max_prefix + S - 1) / S;
+    } else {
+        const int64_t rbs = (R + 63) / 64;
+        const int64_t ctas = (int64_t)B * Hkv * rbs;
+        int64_t S = (4 * (int64_t)sms + ctas - 1) / ctas;
+        if (S < 1) S = 1;
+        chunk = (max_prefix + S - 1) / S;
+    }
+    chunk = (chunk + 127) / 128 * 128;
+    if (chunk < 128) chunk = 128;
+    int64_t S = (max_prefix + chunk - 1) / chunk;
+    if (S < 1) S = 1;
+    pl.S = (int)S;
+    pl.chunk = chunk;
+    const size_t part = (size_t)B * Hkv * S * R;
+    pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float));
+    return pl;
+}
+
+}  // namespace
+}  // namespace rapid
+
+using namespace rapid;
+
+extern "C" {
+
+size_t rapid_verify_attn_workspace_size(int B, int Hq, int Hkv, int d, int n_q,
+                                        int64_t kv_capacity, int dtype) {
+    if (!attn_args_ok(B, Hq, Hkv, d, n_q, kv_capacity, dtype)) return 0;
+    return plan_attn(B, Hq, Hkv, d, n_q, kv_capacity, dtype).ws_bytes;
+}
+
+rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vcache, int dtype,
+                               int B, int Hq, int Hkv, int d, int n_q, int64_t kv_capacity,
+                               const int32_t* prefix_len, const uint8_t* spec_mask,
+                               float softmax_scale, void* O, float* LSE, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    if (!Q || !Kcache || !Vcache || !prefix_len || !O || !LSE || !workspace) return RAPID_EINVAL;
+    if (!attn_args_ok(B, Hq, Hkv, d, n_q, kv_capacity, dtype)) return RAPID_EINVAL;
+    if (!aligned16(Q) || !aligned16(Kcache) || !aligned16(Vcache) || !aligned16(O) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return RAPID_EINVAL;
+    if (!std::isfinite(softmax_scale)) return RAPID_EINVAL;
+    const AttnPlan pl = plan_attn(B, Hq, Hkv, d, n_q, kv_capacity, dtype);
+    if (workspace_bytes < pl.ws_bytes) return RAPID_ENOMEM;
+
+    AttnParams p{};
+    p.Q = Q; p.K = Kcache; p.V = Vcache; p.prefix_len = prefix_len; p.mask = spec_mask;
+    p.O = O; p.LSE = LSE;
+    p.cap = kv_capacity; p.chunk = pl.chunk;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.n_q = n_q; p.G = Hq / Hkv; p.R = p.G * n_q;
+    p.S = pl.S;
+    p.err = device_error_word();
+    p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)d);
+    p.scale_log2 = p.scale * kLog2e;
+    const size_t part = (size_t)B * Hkv * pl.S * p.R;
+    p.part_acc = static_cast<float*>(workspace);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                         align_up(part * d * sizeof(float)));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = pl.tc ? launch_attn_prefix_tc(p, st) : launch_attn_prefix_simt(p, dtype, st);
+    if (e != cudaSuccess) return RAPID_ECUDA;
+    e = launch_attn_merge(p, dtype, st);
+    return e == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
+}
+
+size_t rapid_accept_workspace_size(int B, int n_q, int V) {
+    if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return 0;
+    return align_up((size_t)B * n_q * sizeof(int32_t)) * 2;
+}
+
+rapid_status rapid_accept(const float* z_target, const float* q_draft, const int32_t* draft_tokens,
+                          const int32_t* parent, int B, int n_q, int V, float T, float eta,
+                          uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
+                          int32_t* next_token, int32_t* path, float* diag, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    if (!z_target || !q_draft || !draft_tokens || !n_accepted || !next_token || !workspace)
+        return RAPID_EINVAL;
+    if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return RAPID_EINVAL;
+    if (!(T > 0.f) || !std::isfinite(T) || !(eta >= 0.f) || !std::isfinite(eta)) return RAPID_EINVAL;
+    if ((flags & ~(uint32_t)RAPID_ACCEPT_TAIL_CLAMP) != 0) return RAPID_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(z_target) & 3u) || (reinterpret_cast<uintptr_t>(q_draft) & 3u))
+        return RAPID_EINVAL;
+    const size_t need = rapid_accept_workspace_size(B, n_q, V);
+    if (workspace_bytes < need) return RAPID_ENOMEM;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return RAPID_EINVAL;
+
+    AcceptShape sh = accept_shape(V, 0);
+    if (accept_check_cluster(&sh) != cudaSuccess) return RAPID_EUNSUPPORTED;
+
+    AcceptParams p{};
+    p.z = z_target; p.q = q_draft; p.tokens = draft_tokens; p.parent = parent;
+    p.ws_accept = static_cast<int32_t*>(workspace);
+    p.ws_sample = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
+                                             align_up((size_t)B * n_q * sizeof(int32_t)));
+    p.diag = diag; p.n_accepted = n_accepted; p.next_token = next_token; p.path = path;
+    p.B = B; p.n_q = n_q; p.V = V;
+    p.chunk = sh.chunk;
+    p.bulk = ((V % 4) == 0 && aligned16(z_target) && aligned16(q_draft)) ? 1 : 0;
+    p.clamp = (flags & RAPID_ACCEPT_TAIL_CLAMP) ? 1 : 0;
+    p.invT = 1.0f / T;
+    p.eta = eta;
+    p.seed_lo = (uint32_t)(philox_seed & 0xffffffffu);
+    p.seed_hi = (uint32_t)(philox_seed >> 32);
+    p.err = device_error_word();
+    cudaError_t e = launch_accept(p, sh, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
+}
+
+const char* rapid_status_string(int status) {
+    switch (status) {
+        case RAPID_OK: return "ok";
+        case RAPID_EINVAL: return "invalid argument";
+        case RAPID_ECUDA: return "CUDA error";
+        case RAPID_ENOMEM: return "workspace too small";
+        case RAPID_EUNSUPPORTED: return "unsupported shape";
+        default: return "unknown status";
+    }
+}
+
+int rapid_version(void) { return 100; }
+
+int rapid_device_error(int clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return -1;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+    }
+    return (int)v;
+}
+
+}  // extern "C"

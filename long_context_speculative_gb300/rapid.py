@@ -1,0 +1,180 @@
+"""Thin Python binding of librapid.so (argument marshalling only).
+
+Every step of the verification path runs in the CUDA kernels behind the C
+ABI declared in include/rapid.h; this module only turns torch tensors into
+device pointers, sizes workspaces and passes the current CUDA stream.  There
+is no CPU or PyTorch fallback: if librapid.so is missing or cannot be loaded,
+every call raises.
+"""
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librapid.so")
+
+RAPID_OK = 0
+RAPID_DTYPE_F32 = 0
+RAPID_DTYPE_BF16 = 1
+RAPID_ACCEPT_TAIL_CLAMP = 1
+RAPID_MAX_NQ = 64
+RAPID_MAX_VOCAB = 262144
+
+_lib = None
+
+
+class RapidError(RuntimeError):
+    pass
+
+
+def lib() -> ctypes.CDLL:
+    """Load librapid.so (built by __graft_entry__.build()); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RapidError(f"librapid.so is not built ({LIB_PATH} missing); "
+                         "run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, u32, u64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                       ctypes.c_float, ctypes.c_uint32, ctypes.c_uint64,
+                                       ctypes.c_size_t)
+    L.rapid_verify_attn_workspace_size.argtypes = [i32, i32, i32, i32, i32, i64, i32]
+    L.rapid_verify_attn_workspace_size.restype = sz
+    L.rapid_verify_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, f32,
+                                    vp, vp, vp, sz, vp]
+    L.rapid_verify_attn.restype = i32
+    L.rapid_accept_workspace_size.argtypes = [i32, i32, i32]
+    L.rapid_accept_workspace_size.restype = sz
+    L.rapid_accept.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp, vp, vp,
+                               vp, sz, vp]
+    L.rapid_accept.restype = i32
+    L.rapid_status_string.argtypes = [i32]
+    L.rapid_status_string.restype = ctypes.c_char_p
+    L.rapid_version.argtypes = []
+    L.rapid_version.restype = i32
+    L.rapid_device_error.argtypes = [i32]
+    L.rapid_device_error.restype = i32
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != RAPID_OK:
+        msg = lib().rapid_status_string(status).decode()
+        raise RapidError(f"{what} failed: {msg} ({status})")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise RapidError("librapid works on CUDA tensors only (no CPU path)")
+        if t is not None and not t.is_contiguous():
+            raise RapidError("librapid needs contiguous tensors")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RAPID_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return RAPID_DTYPE_F32
+    raise RapidError(f"unsupported dtype {t.dtype}")
+
+
+# ---------------------------------------------------------------------------
+# C-ABI mirrors (same names, same argument order; tensors in place of pointers)
+# ---------------------------------------------------------------------------
+
+def rapid_verify_attn_workspace_size(B, Hq, Hkv, d, n_q, kv_capacity, dtype) -> int:
+    return int(lib().rapid_verify_attn_workspace_size(B, Hq, Hkv, d, n_q, kv_capacity, dtype))
+
+
+def rapid_verify_attn(Q, Kcache, Vcache, prefix_len, spec_mask, softmax_scale, O, LSE,
+                      workspace, stream=None):
+    """Launch verify attention; shapes are read from the tensors."""
+    _need_cuda(Q, Kcache, Vcache, prefix_len, spec_mask, O, LSE, workspace)
+    B, Hq, n_q, d = Q.shape
+    Hkv, cap = Kcache.shape[1], Kcache.shape[2]
+    st = lib().rapid_verify_attn(_ptr(Q), _ptr(Kcache), _ptr(Vcache), _dtype_code(Q), B, Hq, Hkv,
+                                 d, n_q, cap, _ptr(prefix_len), _ptr(spec_mask),
+                                 float(softmax_scale), _ptr(O), _ptr(LSE), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "rapid_verify_attn")
+
+
+def rapid_accept_workspace_size(B, n_q, V) -> int:
+    return int(lib().rapid_accept_workspace_size(B, n_q, V))
+
+
+def rapid_accept(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, flags,
+                 n_accepted, next_token, path, diag, workspace, stream=None):
+    _need_cuda(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag,
+               workspace)
+    B, n_q, V = z_target.shape
+    st = lib().rapid_accept(_ptr(z_target), _ptr(q_draft), _ptr(draft_tokens), _ptr(parent), B,
+                            n_q, V, float(T), float(eta), int(philox_seed) & ((1 << 64) - 1),
+                            int(flags), _ptr(n_accepted), _ptr(next_token), _ptr(path),
+                            _ptr(diag), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "rapid_accept")
+
+
+def rapid_device_error(clear: bool = True) -> int:
+    return int(lib().rapid_device_error(1 if clear else 0))
+
+
+def rapid_version() -> int:
+    return int(lib().rapid_version())
+
+
+# ---------------------------------------------------------------------------
+# Convenience wrappers that allocate outputs and workspaces with torch
+# ---------------------------------------------------------------------------
+
+def verify_attn(Q, K, V, prefix_len, spec_mask=None, softmax_scale=0.0, out=None, lse=None,
+                workspace=None, stream=None):
+    """O [B,Hq,n_q,d] (dtype of Q) and LSE [B,Hq,n_q] float32."""
+    B, Hq, n_q, d = Q.shape
+    Hkv, cap = K.shape[1], K.shape[2]
+    if out is None:
+        out = torch.empty_like(Q)
+    if lse is None:
+        lse = torch.empty((B, Hq, n_q), dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        nbytes = rapid_verify_attn_workspace_size(B, Hq, Hkv, d, n_q, cap, _dtype_code(Q))
+        if nbytes == 0:
+            raise RapidError("unsupported verify_attn shape")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=Q.device)
+    rapid_verify_attn(Q, K, V, prefix_len, spec_mask, softmax_scale, out, lse, workspace, stream)
+    return out, lse
+
+
+def accept(z, q, tokens, parent=None, T=1.0, eta=1.0, seed=0, tail_clamp=True, want_path=True,
+           want_diag=True, workspace=None, stream=None):
+    """Dict of device tensors n_accepted [B], next_token [B], path [B,n_q], diag [B,n_q,5]."""
+    B, n_q, V = z.shape
+    dev = z.device
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, n_q), dtype=torch.int32, device=dev) if want_path else None
+    diag = torch.empty((B, n_q, 5), dtype=torch.float32, device=dev) if want_diag else None
+    if workspace is None:
+        nbytes = rapid_accept_workspace_size(B, n_q, V)
+        if nbytes == 0:
+            raise RapidError("unsupported accept shape")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flags = RAPID_ACCEPT_TAIL_CLAMP if tail_clamp else 0
+    rapid_accept(z, q, tokens, parent, T, eta, seed, flags, n_acc, nxt, path, diag, workspace,
+                 stream)
+    return dict(n_accepted=n_acc, next_token=nxt, path=path, diag=diag)

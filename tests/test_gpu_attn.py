@@ -1,0 +1,162 @@
+"""Parity of the CUDA verify attention with the oracle (GPU; calls the C ABI).
+
+Inputs come from long_context_speculative_gb300.workloads (seeded); expected
+values from the double-precision oracle on the very same inputs.  Tolerances:
+O absolute 2e-2 (bf16 I/O, fp32 accumulation), LSE absolute 1e-4.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_speculative_gb300 import rapid
+from long_context_speculative_gb300 import workloads as wl
+
+from _parity import check_attn
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _oracle_inputs(a, dtype):
+    if dtype == "bf16":
+        return (wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V), oracle.DTYPE_BF16)
+    return (a.Q.cpu().numpy(), a.K.cpu().numpy(), a.V.cpu().numpy(), oracle.DTYPE_F32)
+
+
+def _run_and_check(w, prefix_override=None, needle=False, capacity=None, mask_none=False,
+                   scale=0.0):
+    a = wl.attn_inputs(w, device=DEV, prefix_override=prefix_override, needle=needle,
+                       capacity=capacity)
+    mask = None if mask_none else a.mask
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, mask, softmax_scale=scale)
+    torch.cuda.synchronize()
+    q, k, v, dt = _oracle_inputs(a, w.dtype)
+    Oo, Lo = oracle.verify_attn(q, k, v, a.prefix_len.cpu().numpy(),
+                                None if mask is None else mask.cpu().numpy(),
+                                scale=None if scale <= 0 else scale, dtype=dt)
+    res = check_attn(O.float().cpu().numpy(), L.cpu().numpy(), Oo, Lo)
+    assert rapid.rapid_device_error(True) == 0
+    return res
+
+
+def test_tiny_fp32_config():
+    err_o, err_l = _run_and_check(wl.TINY)
+    assert err_o < 1e-4   # fp32 end to end: far inside the bf16 tolerance
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("tree", [False, True])
+def test_bf16_small_ragged(d, tree):
+    w = wl.Workload("t", B=3, Hq=8, Hkv=2, d=d, n_q=11 if not tree else 16, prefix=1500,
+                    prefix_lo=200, layers=1, V=10, dtype="bf16", z_std=1, q_noise_std=1,
+                    q_noise_uses_T=True, tree=tree, tree_nodes_max_depth=5, seed=11 + d)
+    _run_and_check(w)
+
+
+def test_bf16_needle_dominated_output():
+    w = wl.Workload("t", B=2, Hq=16, Hkv=4, d=128, n_q=11, prefix=3000, prefix_lo=1000,
+                    layers=1, V=10, dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True,
+                    seed=21)
+    _run_and_check(w, needle=True)
+
+
+@pytest.mark.parametrize("P", [0, 1, 127, 128, 129, 4000])
+def test_edge_prefix_lengths(P):
+    w = wl.Workload("t", B=1, Hq=4, Hkv=1, d=128, n_q=5, prefix=4000, layers=1, V=10,
+                    dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=31)
+    _run_and_check(w, prefix_override=[P])
+
+
+def test_prefix_fills_capacity():
+    w = wl.Workload("t", B=2, Hq=4, Hkv=2, d=128, n_q=7, prefix=1017, layers=1, V=10,
+                    dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=32)
+    # capacity = prefix + n_q exactly: the last speculative row is the last cache row
+    _run_and_check(w, capacity=1024)
+
+
+@pytest.mark.parametrize("G,n_q", [(1, 1), (1, 64), (8, 11), (7, 32), (16, 5)])
+def test_group_widths(G, n_q):
+    w = wl.Workload("t", B=1, Hq=2 * G, Hkv=2, d=128, n_q=n_q, prefix=900, layers=1, V=10,
+                    dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=40 + G)
+    _run_and_check(w)
+
+
+def test_custom_scale_and_fp32_d128():
+    w = wl.Workload("t", B=2, Hq=6, Hkv=3, d=128, n_q=4, prefix=700, prefix_lo=650, layers=1,
+                    V=10, dtype="f32", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=51)
+    _run_and_check(w, scale=0.05)
+
+
+def test_llama8b_layer_32k_all_rows():
+    w = wl.LLAMA8B_LAYER_32K
+    _run_and_check(w)
+
+
+def test_llama8b_120k_layer_sampled_rows():
+    w = wl.LLAMA8B_120K
+    a = wl.attn_inputs(w, device=DEV, layer=3)
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows = np.stack([np.zeros(24, int), rng.integers(0, w.Hq, 24), rng.integers(0, w.n_q, 24)], 1)
+    Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
+                                     a.prefix_len.cpu().numpy(), rows, dtype=oracle.DTYPE_BF16)
+    Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    check_attn(Og, Lg, Oo, Lo)
+
+
+def test_qwen_tree_shape_sampled_rows():
+    w = wl.QWEN7B_TREE
+    a = wl.attn_inputs(w, device=DEV, layer=0)
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, a.mask)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    n = 32
+    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n), rng.integers(0, w.n_q, n)], 1)
+    Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
+                                     a.prefix_len.cpu().numpy(), rows, mask=a.mask.cpu().numpy(),
+                                     dtype=oracle.DTYPE_BF16)
+    Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    check_attn(Og, Lg, Oo, Lo)
+
+
+def test_same_result_twice_and_no_kv_writes():
+    w = wl.Workload("t", B=2, Hq=8, Hkv=2, d=128, n_q=11, prefix=2000, prefix_lo=1500, layers=1,
+                    V=10, dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=61)
+    a = wl.attn_inputs(w, device=DEV)
+    K0, V0 = a.K.clone(), a.V.clone()
+    O1, L1 = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+    O2, L2 = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    assert torch.equal(K0, a.K) and torch.equal(V0, a.V)
+
+
+def test_c_abi_rejects_bad_arguments():
+    L = rapid.lib()
+    Q = torch.zeros((1, 4, 5, 128), dtype=torch.bfloat16, device=DEV)
+    K = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device=DEV)
+    pl = torch.zeros(1, dtype=torch.int32, device=DEV)
+    O = torch.empty_like(Q)
+    lse = torch.empty((1, 4, 5), device=DEV)
+    ws = torch.empty(rapid.rapid_verify_attn_workspace_size(1, 4, 1, 128, 5, 64, 1),
+                     dtype=torch.uint8, device=DEV)
+    p = lambda t: t.data_ptr()
+    args = [p(Q), p(K), p(K), 1, 1, 4, 1, 128, 5, 64, p(pl), None, 0.0, p(O), p(lse), p(ws),
+            ws.numel(), None]
+    assert L.rapid_verify_attn(*args) == 0
+    torch.cuda.synchronize()
+    bad = list(args); bad[7] = 96            # d
+    assert L.rapid_verify_attn(*bad) == -1
+    bad = list(args); bad[5] = 3             # Hq % Hkv with Hkv = 2
+    bad[6] = 2
+    assert L.rapid_verify_attn(*bad) == -1
+    bad = list(args); bad[8] = 65            # n_q
+    assert L.rapid_verify_attn(*bad) == -1
+    bad = list(args); bad[16] = 16           # workspace too small
+    assert L.rapid_verify_attn(*bad) == -3
+    bad = list(args); bad[0] = p(Q) + 2      # misaligned
+    assert L.rapid_verify_attn(*bad) == -1
