@@ -201,6 +201,15 @@ int rapid_version(void);
  */
 int rapid_device_error(int clear);
 
+/*
+ * The full error record of the current device: words8[0] = the sticky bits of
+ * rapid_device_error, words8[1] = 0x80000000 | code of the first wait that
+ * gave up (which kernel role, which barrier, which tile), words8[2..7]
+ * reserved.  Synchronises; clears the record when `clear` is non-zero.
+ * Returns 0 on success, -1 if the record could not be read.
+ */
+int rapid_device_error_info(uint32_t* words8, int clear);
+
 #ifdef __cplusplus
 }
 #endif

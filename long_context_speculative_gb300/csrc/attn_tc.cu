@@ -1,10 +1,484 @@
-// Tensor-core (tcgen05 + TMA) history kernel of verify attention.
+// Tensor-core history kernel of verify attention (bf16, head_dim 128, up to
+// 128 query rows per KV-head group), written for sm_103a: TMA-staged K/V
+// tiles, tcgen05 MMAs with accumulators in tensor memory, warp-specialised.
+//
+// Hybrid tree attention ("LongSpec: Long-Context Lossless Speculative
+// Decoding with Efficient Drafting and Verification", section 2.3) needs no
+// mask over the history rows: every query of the group sees every history
+// row, so the history pass is a plain split-KV flash-decoding pass.  The GQA
+// group's G * n_q query rows form the M = 128 operand of one tcgen05 MMA, so
+// every K/V byte is read from HBM once per group.
+//
+// CTA = (split s, sequence b * Hkv + KV head g); 192 threads:
+//   warps 0-3  softmax: thread t owns query row t (TMEM lane t).  Loads Q into
+//              shared memory, turns each S tile into P (bf16) in shared
+//              memory, keeps the running max / sum, rescales O in TMEM when
+//              the max grows by more than 2^8, writes the split's partial.
+//   warp 4     TMA producer: 64-key K and V tiles into a 4-stage ring.
+//   warp 5     allocates TMEM and issues the MMAs (one elected thread):
+//              S_i = Q K_i^T (M128 N64 K128) into a double-buffered S, and
+//              O += P_i V_i (M128 N128 K64).
+// Shared-memory operands use the 128-byte swizzle; Q, K and P are K-major,
+// V is MN-major (d contiguous).  Every mbarrier wait is bounded; on a timeout
+// the kernel records an error bit, stops issuing work, drains what it issued
+// and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "attn.cuh"
+#include "common.cuh"
 
 namespace rapid {
 
-bool attn_prefix_tc_supported(const AttnParams&, int) { return false; }
+namespace {
 
-cudaError_t launch_attn_prefix_tc(const AttnParams&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int kThreads = 192;
+constexpr int kD = 128;
+constexpr int kKeys = 64;                       // keys per K/V tile
+constexpr int kStages = 4;
+constexpr uint32_t kTmemCols = 256;             // S0 [0,64) S1 [64,128) O [128,256)
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 128;
+
+constexpr int kQBytes = 128 * kD * 2;           // 2 column blocks x 16 KB
+constexpr int kPBytes = 128 * kKeys * 2;        // 16 KB
+constexpr int kTileBytes = kKeys * kD * 2;      // 16 KB: 2 column blocks x 8 KB
+constexpr int kStageBytes = 2 * kTileBytes;     // K + V
+constexpr int kOffQ = 0;
+constexpr int kOffP = kOffQ + kQBytes;
+constexpr int kOffKV = kOffP + kPBytes;
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + 1 KB alignment slack
+
+// Instruction descriptors (kind::f16): D = f32 (bits 4-5 = 1), A = B = bf16
+// (bits 7-9 = 1, bits 10-12 = 1), bit 15/16 = A/B MN-major, bits 17-22 = N/8,
+// bits 24-28 = M/16.
+constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKeys >> 3) << 17) |
+                             ((uint32_t)(128 >> 4) << 24);
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                              ((uint32_t)(kD >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), version 1 (bits 46-47), 128-byte swizzle (bits 61-63 = 2).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Codes recorded by a timed-out wait: role << 24 | barrier << 16 | tile.
+enum : unsigned int {
+    kRoleProducer = 1u << 24, kRoleMma = 2u << 24, kRoleSoftmax = 3u << 24,
+    kBarKvFull = 1u << 16, kBarKvEmpty = 2u << 16, kBarSFull = 3u << 16,
+    kBarPFull = 4u << 16, kBarPFree = 5u << 16, kBarDrain = 6u << 16
+};
+
+struct Bars {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2];
+    uint64_t p_full;
+    uint64_t p_free;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment of the shared-window address (128-byte swizzle atoms).
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int s = blockIdx.x;
+    const int bg = blockIdx.y;
+    const int b = bg / p.Hkv;
+    const int g = bg - b * p.Hkv;
+
+    // Tiles of this split: the history [0, P) in 64-key tiles, shared out
+    // evenly over the S splits of this (b, g).
+    const int64_t P = clamped_prefix(p, b);
+    const int n_all = (int)((P + kKeys - 1) / kKeys);
+    const int t_begin = (int)(((int64_t)s * n_all) / p.S);
+    const int t_end = (int)(((int64_t)(s + 1) * n_all) / p.S);
+    const int n = t_end - t_begin;
+    const int64_t slot = ((int64_t)bg * p.S + s) * p.R;
+
+    if (n <= 0) {   // empty split: m = -inf, l = 0 (no tile touched)
+        if (tid < p.R) {
+            p.part_ml[(slot + tid) * 2 + 0] = -INFINITY;
+            p.part_ml[(slot + tid) * 2 + 1] = 0.f;
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bars->kv_full[i], 1);
+            mbar_init(&bars->kv_empty[i], 1);
+        }
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->s_full[1], 1);
+        mbar_init(&bars->p_full, 128);
+        mbar_init(&bars->p_free, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars->tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Q rows of the group into shared memory (K-major, 128-byte swizzle);
+    // rows >= R are zero.
+    if (tid < 128) {
+        const int r = tid;
+        uint4 chunk[16];
+        if (r < p.R) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.Q) +
+                (((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q + r) * kD);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) chunk[j] = src[j];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) chunk[j] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int blk = j >> 3, jj = j & 7;
+            *reinterpret_cast<uint4*>(smem + kOffQ + blk * (128 * 128) + r * 128 +
+                                      ((jj ^ (r & 7)) << 4)) = chunk[j];
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t smem_base = smem_u32(smem);
+    const int64_t head_row0 = (int64_t)bg * p.cap;
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer --------------------------
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(&bars->kv_empty[st], ((i / kStages) + 1) & 1, p.err,
+                               kRoleProducer | kBarKvEmpty | (unsigned)(i & 0xffff))) {
+                    bars->abort = 1;
+                    break;
+                }
+                if (*((volatile int*)&bars->abort)) break;
+                ++issued;
+                uint8_t* kt = smem + kOffKV + st * kStageBytes;
+                uint8_t* vt = kt + kTileBytes;
+                const int y = (int)(head_row0 + (int64_t)(t_begin + i) * kKeys);
+                mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
+                tma_load_2d(kt, &tmK, 0, y, &bars->kv_full[st]);
+                tma_load_2d(kt + kTileBytes / 2, &tmK, 64, y, &bars->kv_full[st]);
+                tma_load_2d(vt, &tmV, 0, y, &bars->kv_full[st]);
+                tma_load_2d(vt + kTileBytes / 2, &tmV, 64, y, &bars->kv_full[st]);
+            }
+            if (*((volatile int*)&bars->abort)) {
+                // let the copies still in flight land before the CTA exits
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&bars->kv_full[i % kStages], (i / kStages) & 1, p.err,
+                              kRoleProducer | kBarKvFull | (unsigned)(i & 0xffff));
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer ----------------------------
+        if (lane == 0) {
+            const uint32_t qaddr = smem_base + kOffQ;
+            const uint32_t paddr = smem_base + kOffP;
+            auto issue_s = [&](int i) -> bool {
+                const int st = i % kStages;
+                if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, p.err,
+                               kRoleMma | kBarKvFull | (unsigned)(i & 0xffff)))
+                    return false;
+                tc_fence_after();
+                const uint32_t kaddr = smem_base + kOffKV + st * kStageBytes;
+                const uint32_t dS = tmem + kTmemS + (uint32_t)((i & 1) * kKeys);
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t off = (uint32_t)((k >> 2) * (128 * 128) + (k & 3) * 32);
+                    const uint32_t koff = (uint32_t)((k >> 2) * (kKeys * 128) + (k & 3) * 32);
+                    mma_bf16(dS, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + koff, 16, 1024),
+                             kIdescS, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->s_full[i & 1]);
+                return true;
+            };
+            bool ok = issue_s(0);
+            for (int i = 0; ok && i < n; ++i) {
+                if (i + 1 < n && !issue_s(i + 1)) { ok = false; break; }
+                if (!mbar_wait(&bars->p_full, i & 1, p.err,
+                               kRoleMma | kBarPFull | (unsigned)(i & 0xffff))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int st = i % kStages;
+                const uint32_t vaddr = smem_base + kOffKV + st * kStageBytes + kTileBytes;
+#pragma unroll
+                for (int k = 0; k < kKeys / 16; ++k) {
+                    mma_bf16(tmem + kTmemO, sdesc(paddr + k * 32, 16, 1024),
+                             sdesc(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
+                             (i > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->p_free);
+                mma_commit(&bars->kv_empty[st]);
+            }
+            if (!ok) bars->abort = 1;
+            // drain: every MMA issued so far has completed once this arrives
+            mma_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0, p.err, kRoleMma | kBarDrain);
+        }
+    } else {
+        // ------------------------------ softmax warps -------------------------
+        const int r = tid;                                    // query row = TMEM lane
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const float c = p.scale_log2;
+        const int64_t key_end = ((int64_t)t_end * kKeys < P) ? (int64_t)t_end * kKeys : P;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int i = 0; i < n; ++i) {
+            const bool got_s = mbar_wait(&bars->s_full[i & 1], (i >> 1) & 1, p.err,
+                                         kRoleSoftmax | kBarSFull | (unsigned)(i & 0xffff));
+            if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld32(lane_addr + kTmemS + (uint32_t)((i & 1) * kKeys), sr[0]);
+            tmem_ld32(lane_addr + kTmemS + (uint32_t)((i & 1) * kKeys) + 32, sr[1]);
+            tmem_wait_ld();
+            const int64_t key0 = (int64_t)(t_begin + i) * kKeys;
+            const int nvalid = (key_end - key0 < kKeys) ? (int)(key_end - key0) : kKeys;
+            float sv[64];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float x = (j < nvalid) ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
+                sv[j] = x;
+                mx = fmaxf(mx, x);
+            }
+            const float mt = mx * c;
+            float corr = 1.f;
+            bool rescale = false;
+            if (mt > m_run + 8.f) {               // also true for the first tile
+                corr = exp2f(m_run - mt);         // 0 when m_run = -inf
+                rescale = (i > 0);
+                m_run = mt;
+            }
+            float sum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = exp2f(fmaf(sv[2 * j], c, -m_run));
+                const float p1 = exp2f(fmaf(sv[2 * j + 1], c, -m_run));
+                sum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l_run = l_run * corr + sum;
+            // PV of the previous tile must be done: it reads the P buffer and
+            // accumulates into O.
+            const bool got_free =
+                (i == 0) || mbar_wait(&bars->p_free, (i - 1) & 1, p.err,
+                                      kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff));
+            if (!__all_sync(0xffffffffu, got_free)) { ok = false; break; }
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int q = 0; q < kD / 32; ++q) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
+                    tmem_st32(lane_addr + kTmemO + q * 32, o);
+                }
+                tmem_wait_st();
+            }
+            uint8_t* prow = smem + kOffP + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full);
+        }
+        const bool got_last = ok && mbar_wait(&bars->p_free, (n - 1) & 1, p.err,
+                                              kRoleSoftmax | kBarPFree | 0xffffu);
+        if (__all_sync(0xffffffffu, got_last)) {
+            tc_fence_after();
+            // tcgen05.ld is warp-collective (.sync.aligned): every lane of the
+            // warp executes the same load instruction; only the stores depend
+            // on whether this lane's row is a real query row.
+            const bool real_row = r < p.R;
+            float* dst = p.part_acc + (slot + r) * kD;
+#pragma unroll
+            for (int q = 0; q < kD / 32; ++q) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                tmem_wait_ld();
+                if (real_row) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(dst + q * 32 + j) =
+                            make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                                        __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                }
+            }
+            if (real_row) {
+                p.part_ml[(slot + r) * 2 + 0] = m_run;
+                p.part_ml[(slot + r) * 2 + 1] = l_run;
+            }
+        } else {
+            bars->abort = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D view [rows, 128] of a bf16 KV cache; 64 x 64 boxes, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kKeys};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
+    if (dtype != 1 || p.d != kD) return false;
+    if (p.R < 1 || p.R > 128) return false;
+    if ((int64_t)p.B * p.Hkv * p.cap >= ((int64_t)1 << 31)) return false;
+    return tensor_map_encoder() != nullptr;
+}
+
+cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)p.B * p.Hkv * p.cap;
+    if (!make_kv_map(&tmK, p.K, rows) || !make_kv_map(&tmV, p.V, rows))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.S, p.B * p.Hkv);
+    attn_prefix_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmK, tmV, p);
+    return cudaGetLastError();
+}
 
 }  // namespace rapid

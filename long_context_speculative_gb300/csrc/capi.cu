@@ -10,7 +10,8 @@
 
 namespace rapid {
 
-__device__ unsigned int g_device_error = 0;
+// [0] sticky error bits, [1] code of the first timed-out wait, [2..7] spare.
+__device__ unsigned int g_device_error[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 
 namespace {
 
@@ -194,13 +195,21 @@ const char* rapid_status_string(int status) {
 int rapid_version(void) { return 100; }
 
 int rapid_device_error(int clear) {
-    unsigned int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return -1;
+    uint32_t w[8];
+    if (rapid_device_error_info(w, clear) != 0) return -1;
+    return (int)w[0];
+}
+
+int rapid_device_error_info(uint32_t* words8, int clear) {
+    unsigned int v[8];
+    if (cudaMemcpyFromSymbol(v, g_device_error, sizeof(v)) != cudaSuccess) return -1;
     if (clear) {
-        const unsigned int zero = 0;
-        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return -1;
+        const unsigned int zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (cudaMemcpyToSymbol(g_device_error, zero, sizeof(zero)) != cudaSuccess) return -1;
     }
-    return (int)v;
+    if (words8)
+        for (int i = 0; i < 8; ++i) words8[i] = v[i];
+    return 0;
 }
 
 }  // extern "C"

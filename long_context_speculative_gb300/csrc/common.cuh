@@ -101,11 +101,13 @@ RAPID_DEVICE void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Non-blocking test of phase `parity` (mbarrier.test_wait never suspends the
+// thread, so a caller's own time limit really bounds the wait).
 RAPID_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
@@ -113,14 +115,32 @@ RAPID_DEVICE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls (each poll may suspend the
-// thread for a hardware-defined interval), records kErrWaitTimeout and
-// returns false.  Every wait on an mbarrier in this library goes through it.
+RAPID_DEVICE uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Default wall-clock bound of one wait.  Legitimate waits last microseconds;
+// one second means the producer of the phase is gone.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Bounded wait on phase `parity` of an mbarrier: gives up after `limit_ns` of
+// wall-clock time (globaltimer), records kErrWaitTimeout in err[0] and, if it
+// is the first failure, `code` in err[1], and returns false.  Every wait on an
+// mbarrier in this library goes through it.
 RAPID_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
-                            uint32_t limit = (1u << 22)) {
-    for (uint32_t it = 0; it < limit; ++it)
+                            unsigned int code = 0, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-    if (err) atomicOr(err, kErrWaitTimeout);
+        if (global_timer_ns() - t0 > limit_ns) break;
+    }
+    if (err) {
+        atomicOr(err, kErrWaitTimeout);
+        atomicCAS(err + 1, 0u, code | 0x80000000u);
+    }
     return false;
 }
 

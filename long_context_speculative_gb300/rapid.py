@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
     L.rapid_version.restype = i32
     L.rapid_device_error.argtypes = [i32]
     L.rapid_device_error.restype = i32
+    L.rapid_device_error_info.argtypes = [vp, i32]
+    L.rapid_device_error_info.restype = i32
     _lib = L
     return L
 
@@ -132,6 +134,13 @@ def rapid_accept(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, f
 
 def rapid_device_error(clear: bool = True) -> int:
     return int(lib().rapid_device_error(1 if clear else 0))
+
+
+def rapid_device_error_info(clear: bool = True):
+    words = (ctypes.c_uint32 * 8)()
+    if lib().rapid_device_error_info(ctypes.cast(words, ctypes.c_void_p), 1 if clear else 0) != 0:
+        raise RapidError("could not read the device error record")
+    return list(words)
 
 
 def rapid_version() -> int:
