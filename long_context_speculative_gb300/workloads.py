@@ -64,6 +64,9 @@ LLAMA8B_LAYER_32K = Workload("llama3.1-8b_layer_32k", B=1, Hq=32, Hkv=8, d=128, 
 LLAMA8B_120K = Workload("llama3.1-8b_32layers_120k", B=1, Hq=32, Hkv=8, d=128, n_q=11,
                         prefix=122880, layers=32, V=128256, dtype="bf16", z_std=3.0,
                         q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0, seed=1003)
+LLAMA8B_1LAYER_120K = Workload("llama3.1-8b_1layer_120k", B=1, Hq=32, Hkv=8, d=128, n_q=11,
+                               prefix=122880, layers=1, V=128256, dtype="bf16", z_std=3.0,
+                               q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0, seed=1006)
 LLAMA70B_128K = Workload("llama3.1-70b_80layers_128k", B=1, Hq=64, Hkv=8, d=128, n_q=11,
                          prefix=131072, layers=80, V=128256, dtype="bf16", z_std=3.0,
                          q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0, seed=1004)
@@ -72,7 +75,7 @@ QWEN7B_TREE = Workload("qwen2.5-7b_tree32_28layers", B=4, Hq=28, Hkv=4, d=128, n
                        z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
                        tree=True, seed=1005)
 
-ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA70B_128K, QWEN7B_TREE]
+ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA8B_1LAYER_120K, LLAMA70B_128K, QWEN7B_TREE]
 
 
 def gen(seed: int, device="cpu") -> torch.Generator:
