@@ -107,6 +107,7 @@ accept_rows_kernel(const AcceptParams p) {
     float* sz = reinterpret_cast<float*>(dyn_f4);
     float* sq = sz + p.chunk;
     __shared__ RowShared sh;
+    griddep_wait();
 
     const int64_t lo = (int64_t)rank * p.chunk;
     int64_t n64 = (int64_t)p.V - lo;
@@ -238,6 +239,8 @@ accept_rows_kernel(const AcceptParams p) {
             if (tok < 0 || tok >= p.V) p.ws_accept[(int64_t)b * p.n_q + node] = 0;
         }
     }
+
+    if (t == 0) griddep_launch_dependents();
 
     // ---- pass 3: candidate next token of this row ------------------------
     const Philox4 rnd = philox4x32_10((uint32_t)(j + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
@@ -391,6 +394,7 @@ accept_rows_kernel(const AcceptParams p) {
 
 // One thread per sequence: pick the winning path and the next token.
 __global__ void accept_select_kernel(const AcceptParams p) {
+    griddep_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= p.B) return;
     const int n_q = p.n_q;
@@ -438,13 +442,15 @@ cudaError_t launch_rows(const AcceptParams& p, int C, cudaStream_t st) {
     cfg.blockDim = dim3(kNT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -543,8 +549,16 @@ cudaError_t launch_accept(const AcceptParams& p, const AcceptShape& sh, cudaStre
     cudaError_t e = launch_rows_dispatch(sh.F, p, sh.cluster, st);
     if (e != cudaSuccess) return e;
     const int threads = 64;
-    accept_select_kernel<<<(p.B + threads - 1) / threads, threads, 0, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.B + threads - 1) / threads, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_select_kernel, p);
 }
 
 }  // namespace rapid

@@ -21,12 +21,14 @@ struct AttnParams {
     const uint8_t* mask;  // [B, n_q, n_q] or nullptr (chain)
     void* O;              // [B, Hq, n_q, d]
     float* LSE;           // [B, Hq, n_q]
-    float* part_acc;      // [B*Hkv, S, R, d]   un-normalised partial outputs
-    float* part_ml;       // [B*Hkv, S, R, 2]   (running max m, sum l), log2 domain
+    float* part_acc;      // [B*Hkv, nparts, R, d]   un-normalised partial outputs
+    float* part_ml;       // [B*Hkv, nparts, R, 2]   (running max m, sum l), log2 domain
     unsigned int* err;    // sticky device error word
     int64_t cap;          // KV rows per head
     int64_t chunk;        // history rows per split (multiple of 128)
     int B, Hq, Hkv, d, n_q, G, R, S;
+    int spec_in_partials; // 1: the history kernel already attended the speculative rows
+    int nparts;           // partial slots per (b, KV head): S, or 2 S for the tensor-core kernel
     float scale;          // softmax scale (natural units)
     float scale_log2;     // scale * log2(e)
 };

@@ -58,6 +58,7 @@ attn_prefix_simt_kernel(const AttnParams p) {
     float* sK = sQ + kSimtRows * D;                  // [32][DP]
     float* sV = sK + kSimtKeys * DP;                 // [32][D]
 
+    griddep_wait();
     const int s = blockIdx.x;
     const int rb = blockIdx.y;
     const int bg = blockIdx.z;
@@ -160,7 +161,7 @@ attn_prefix_simt_kernel(const AttnParams p) {
     }
 
     // Partial of this split: acc, (m, l).  An empty split leaves m = -inf, l = 0.
-    const int64_t slot = ((int64_t)bg * p.S + s) * p.R;
+    const int64_t slot = ((int64_t)bg * p.nparts + s) * p.R;
 #pragma unroll
     for (int i = 0; i < kSimtRowsPerWarp; ++i) {
         const int r = warp + 4 * i;
@@ -175,16 +176,25 @@ attn_prefix_simt_kernel(const AttnParams p) {
     }
 }
 
-// One warp per query row (b, h, i): masked attention over the n_q speculative
-// rows, then the log-sum-exp merge with the S history partials:
+// One warp per query row (b, h, i), 8 rows per CTA: masked attention over the
+// n_q speculative rows, then the log-sum-exp merge with the S history partials:
 //   M = max(m_spec, m_s);  L = sum_parts l_part 2^(m_part - M);
 //   O = sum_parts acc_part 2^(m_part - M) / L;   LSE = (M + log2 L) ln 2.
+// Latency-tolerant: the S (m, l) pairs are read in one coalesced sweep, the
+// split weights go through shared memory, and the partial rows are loaded
+// with independent, unrolled loads.
+constexpr int kMergeRows = 8;
+constexpr int kMergeMaxS = 1024;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
     constexpr int NC = D / 32;
+    __shared__ float s_w[kMergeRows][kMergeMaxS + 64];   // split weights, then spec scores
+    griddep_wait();
+    griddep_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * 4 + warp;
+    const int r = blockIdx.x * kMergeRows + warp;
     const int bg = blockIdx.y;
     if (r >= p.R) return;
     const int b = bg / p.Hkv;
@@ -192,58 +202,87 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(const AttnParams p) {
     const int h = g * p.G + r / p.n_q;
     const int i = r % p.n_q;
     const int64_t P = clamped_prefix(p, b);
+    float* wsm = s_w[warp];
+    float* ssc = s_w[warp] + kMergeMaxS;
 
     const T* Qrow = static_cast<const T*>(p.Q) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
     const T* Kh = static_cast<const T*>(p.K) + (int64_t)bg * p.cap * D;
     const T* Vh = static_cast<const T*>(p.V) + (int64_t)bg * p.cap * D;
 
-    float q[NC], acc[NC];
+    // ---- speculative rows: scores (log2 domain) of the visible ones --------
+    // (skipped when the history kernel already folded them into a partial)
+    const int n_spec = p.spec_in_partials ? 0 : p.n_q;
+    float q[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) {
-        q[c] = to_float(Qrow[lane + 32 * c]) * p.scale_log2;
-        acc[c] = 0.f;
-    }
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < p.n_q; ++j) {
+    for (int c = 0; c < NC; ++c) q[c] = to_float(Qrow[lane + 32 * c]) * p.scale_log2;
+    float m_spec = -INFINITY;
+    for (int j = 0; j < n_spec; ++j) {
         const bool vis = p.mask ? (p.mask[((int64_t)b * p.n_q + i) * p.n_q + j] != 0) : (j <= i);
-        if (!vis) continue;
-        const T* kr = Kh + (P + j) * D;
-        const T* vr = Vh + (P + j) * D;
         float dot = 0.f;
+        if (vis) {
+            const T* kr = Kh + (P + j) * D;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) dot = fmaf(q[c], to_float(kr[lane + 32 * c]), dot);
-        const float sj = warp_sum(dot);
-        const float mnew = fmaxf(m, sj);
-        const float corr = exp2f(m - mnew);
-        const float pj = exp2f(sj - mnew);
-        l = l * corr + pj;
-        m = mnew;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = fmaf(pj, to_float(vr[lane + 32 * c]), acc[c] * corr);
+            for (int c = 0; c < NC; ++c) dot = fmaf(q[c], to_float(kr[lane + 32 * c]), dot);
+        }
+        const float sj = vis ? warp_sum(dot) : -INFINITY;   // vis is warp-uniform
+        if (lane == 0) ssc[j] = sj;
+        m_spec = fmaxf(m_spec, sj);
     }
-
-    const float* ml = p.part_ml + ((int64_t)bg * p.S) * p.R * 2;
-    const float* pa = p.part_acc + ((int64_t)bg * p.S) * p.R * D;
-    float M = m;
-    for (int s = 0; s < p.S; ++s) {
-        const float ls = ml[((int64_t)s * p.R + r) * 2 + 1];
-        if (ls > 0.f) M = fmaxf(M, ml[((int64_t)s * p.R + r) * 2]);
+    // ---- history splits: (m, l) in one sweep --------------------------------
+    const int nparts = p.nparts;
+    const float* ml = p.part_ml + ((int64_t)bg * nparts) * p.R * 2;
+    float M = m_spec;
+    for (int s0 = lane; s0 < nparts; s0 += 32) {
+        const float ls = ml[((int64_t)s0 * p.R + r) * 2 + 1];
+        const float ms = ml[((int64_t)s0 * p.R + r) * 2];
+        if (ls > 0.f) M = fmaxf(M, ms);
     }
-    float L = 0.f;
-    if (l > 0.f) {
-        const float w = exp2f(m - M);
-        L = l * w;
-#pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] *= w;
+    M = warp_max(M);
+    float Lpart = 0.f;
+    for (int s0 = lane; s0 < nparts; s0 += 32) {
+        const float ls = ml[((int64_t)s0 * p.R + r) * 2 + 1];
+        const float ms = ml[((int64_t)s0 * p.R + r) * 2];
+        const float w = ls > 0.f ? exp2f(ms - M) : 0.f;
+        wsm[s0] = w;
+        Lpart = fmaf(ls, w, Lpart);
     }
-    for (int s = 0; s < p.S; ++s) {
-        const float ls = ml[((int64_t)s * p.R + r) * 2 + 1];
-        if (!(ls > 0.f)) continue;
-        const float w = exp2f(ml[((int64_t)s * p.R + r) * 2] - M);
-        L = fmaf(ls, w, L);
-        const float* src = pa + ((int64_t)s * p.R + r) * D;
+    float L = warp_sum(Lpart);
+    __syncwarp();
+    float acc[NC];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = fmaf(src[lane + 32 * c], w, acc[c]);
+    for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+    // speculative V rows
+    for (int j = 0; j < n_spec; ++j) {
+        const float sj = ssc[j];
+        if (sj == -INFINITY) continue;                        // warp-uniform
+        const float w = exp2f(sj - M);
+        L += w;
+        const T* vr = Vh + (P + j) * D;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, to_float(vr[lane + 32 * c]), acc[c]);
+    }
+    // history partials
+    const float* pa = p.part_acc + ((int64_t)bg * nparts) * p.R * D + (int64_t)r * D + lane;
+    const int64_t sstride = (int64_t)p.R * D;
+    int s0 = 0;
+    for (; s0 + 4 <= nparts; s0 += 4) {
+        float v[4][NC];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int c = 0; c < NC; ++c) v[u][c] = pa[(s0 + u) * sstride + 32 * c];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = wsm[s0 + u];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, w != 0.f ? v[u][c] : 0.f, acc[c]);
+        }
+    }
+    for (; s0 < nparts; ++s0) {
+        const float w = wsm[s0];
+        if (w == 0.f) continue;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, pa[s0 * sstride + 32 * c], acc[c]);
     }
 
     T* Orow = static_cast<T*>(p.O) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
@@ -267,9 +306,17 @@ cudaError_t launch_simt_typed(const AttnParams& p, cudaStream_t st) {
 
 template <typename T, int D>
 cudaError_t launch_merge_typed(const AttnParams& p, cudaStream_t st) {
-    dim3 grid((p.R + 3) / 4, p.B * p.Hkv);
-    attn_merge_kernel<T, D><<<grid, 128, 0, st>>>(p);
-    return cudaGetLastError();
+    if (p.nparts > kMergeMaxS) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.R + kMergeRows - 1) / kMergeRows, p.B * p.Hkv, 1);
+    cfg.blockDim = dim3(32 * kMergeRows, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_merge_kernel<T, D>, p);
 }
 
 }  // namespace

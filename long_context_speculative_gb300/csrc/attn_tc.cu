@@ -9,19 +9,24 @@
 // group's G * n_q query rows form the M = 128 operand of one tcgen05 MMA, so
 // every K/V byte is read from HBM once per group.
 //
-// CTA = (split s, sequence b * Hkv + KV head g); 192 threads:
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t).  Loads Q into
-//              shared memory, turns each S tile into P (bf16) in shared
-//              memory, keeps the running max / sum, rescales O in TMEM when
-//              the max grows by more than 2^8, writes the split's partial.
-//   warp 4     TMA producer: 64-key K and V tiles into a 4-stage ring.
-//   warp 5     allocates TMEM and issues the MMAs (one elected thread):
-//              S_i = Q K_i^T (M128 N64 K128) into a double-buffered S, and
-//              O += P_i V_i (M128 N128 K64).
+// CTA = (split s, sequence b * Hkv + KV head g); 320 threads:
+//   warps 0-7  softmax, in two consumer groups (warps 0-3 take the even
+//              tiles of the split, warps 4-7 the odd ones); warp w owns TMEM
+//              lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.  A
+//              group turns its S tile into P (bf16, its own shared buffer),
+//              keeps its running max / sum and rescales its O in TMEM when the
+//              max grows by more than 2^8.  Each group leaves its own partial
+//              (the merge combines them like any other split).
+//   warp 8     TMA producer: 64-key K and V tiles into a 4-stage ring; the
+//              last split also loads the n_q speculative rows as one more
+//              tile, which the softmax masks with the chain / tree mask.
+//   warp 9     allocates TMEM and issues the MMAs (one thread), in the order
+//              their inputs become ready: S_j = Q K_j^T (M128 N64 K128) and
+//              O_g += P_i V_i (M128 N128 K64).
 // Shared-memory operands use the 128-byte swizzle; Q, K and P are K-major,
-// V is MN-major (d contiguous).  Every mbarrier wait is bounded; on a timeout
-// the kernel records an error bit, stops issuing work, drains what it issued
-// and returns.
+// V is MN-major (d contiguous).  Every mbarrier wait is bounded in wall-clock
+// time; on a timeout the kernel records an error code, stops issuing work,
+// drains what it issued and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,23 +37,28 @@ namespace rapid {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;                // two per TMEM lane quadrant
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kD = 128;
 constexpr int kKeys = 64;                       // keys per K/V tile
 constexpr int kStages = 4;
-constexpr uint32_t kTmemCols = 256;             // S0 [0,64) S1 [64,128) O [128,256)
+constexpr uint32_t kTmemCols = 512;   // S of group 0/1: [0,64) [64,128); O of group 0/1: [128,256) [256,384)
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
 
 constexpr int kQBytes = 128 * kD * 2;           // 2 column blocks x 16 KB
-constexpr int kPBytes = 128 * kKeys * 2;        // 16 KB
+constexpr int kPBytes = 128 * kKeys * 2;        // 16 KB per P buffer (two buffers)
 constexpr int kTileBytes = kKeys * kD * 2;      // 16 KB: 2 column blocks x 8 KB
 constexpr int kStageBytes = 2 * kTileBytes;     // K + V
 constexpr int kOffQ = 0;
 constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffKV = kOffP + kPBytes;
+constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + 1 KB alignment slack
+constexpr int kBarBytes = 256;
+constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + 1 KB alignment slack
 
 // Instruction descriptors (kind::f16): D = f32 (bits 4-5 = 1), A = B = bf16
 // (bits 7-9 = 1, bits 10-12 = 1), bit 15/16 = A/B MN-major, bits 17-22 = N/8,
@@ -133,6 +143,14 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x with the SFU instruction (flushes denormal results to zero; P is
+// rounded to bf16 afterwards and the running sums tolerate the 2-ulp error).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -149,13 +167,14 @@ enum : unsigned int {
 struct Bars {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full;
-    uint64_t p_free;
+    uint64_t s_full[2];   // S of consumer group g written
+    uint64_t p_full[2];   // P of group g written (kSoftmaxThreads / 2 arrivals)
+    uint64_t p_free[2];   // PV product of group g done
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= kBarBytes, "barrier block too small");
 
 __global__ void __launch_bounds__(kThreads, 1)
 attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -173,46 +192,46 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
 
-    // Tiles of this split: the history [0, P) in 64-key tiles, shared out
-    // evenly over the S splits of this (b, g).
-    const int64_t P = clamped_prefix(p, b);
-    const int n_all = (int)((P + kKeys - 1) / kKeys);
-    const int t_begin = (int)(((int64_t)s * n_all) / p.S);
-    const int t_end = (int)(((int64_t)(s + 1) * n_all) / p.S);
-    const int n = t_end - t_begin;
-    const int64_t slot = ((int64_t)bg * p.S + s) * p.R;
-
-    if (n <= 0) {   // empty split: m = -inf, l = 0 (no tile touched)
-        if (tid < p.R) {
-            p.part_ml[(slot + tid) * 2 + 0] = -INFINITY;
-            p.part_ml[(slot + tid) * 2 + 1] = 0.f;
-        }
-        return;
-    }
-
+    // Input-free set-up first: it may overlap the previous kernel in the stream.
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&bars->kv_full[i], 1);
             mbar_init(&bars->kv_empty[i], 1);
         }
-        mbar_init(&bars->s_full[0], 1);
-        mbar_init(&bars->s_full[1], 1);
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->p_free, 1);
+        for (int gr = 0; gr < 2; ++gr) {
+            mbar_init(&bars->s_full[gr], 1);
+            mbar_init(&bars->p_full[gr], kSoftmaxThreads / 2);
+            mbar_init(&bars->p_free[gr], 1);
+        }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&bars->tmem_base)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    griddep_wait();
+
+    // Tiles of this split: the history [0, P) in 64-key tiles, shared out
+    // evenly over the S splits of this (b, g); the last split also takes the
+    // n_q speculative rows [P, P + n_q) as one more, masked, tile.  Tile i is
+    // processed by consumer group i & 1; each group leaves its own partial.
+    const int64_t P = clamped_prefix(p, b);
+    const int n_all = (int)((P + kKeys - 1) / kKeys);
+    const int t_begin = (int)(((int64_t)s * n_all) / p.S);
+    const int t_end = (int)(((int64_t)(s + 1) * n_all) / p.S);
+    const int n_hist = t_end - t_begin;
+    const bool spec_here = (s == p.S - 1);
+    const int n = n_hist + (spec_here ? 1 : 0);
+    const int64_t slot0 = ((int64_t)bg * p.nparts + 2 * s) * p.R;   // group g: slot0 + g * R
+
     // Q rows of the group into shared memory (K-major, 128-byte swizzle);
     // rows >= R are zero.
-    if (tid < 128) {
+    if (tid < 128 && n > 0) {
         const int r = tid;
         uint4 chunk[16];
         if (r < p.R) {
@@ -233,6 +252,14 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
         fence_proxy_async_smem();
     }
+    // A group without tiles leaves an empty partial: m = -inf, l = 0.
+    if (tid < 2 * 128) {
+        const int gr = tid >> 7, r = tid & 127;
+        if (gr >= n && r < p.R) {
+            p.part_ml[(slot0 + gr * p.R + r) * 2 + 0] = -INFINITY;
+            p.part_ml[(slot0 + gr * p.R + r) * 2 + 1] = 0.f;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -240,15 +267,17 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const uint32_t smem_base = smem_u32(smem);
     const int64_t head_row0 = (int64_t)bg * p.cap;
 
-    if (warp == 4) {
+    if (n <= 0) {
+        // nothing else to do
+    } else if (warp == kProducerWarp) {
         // ------------------------------ TMA producer --------------------------
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < n; ++i) {
                 const int st = i % kStages;
                 if (i >= kStages &&
-                    !mbar_wait(&bars->kv_empty[st], ((i / kStages) + 1) & 1, p.err,
-                               kRoleProducer | kBarKvEmpty | (unsigned)(i & 0xffff))) {
+                    !mbar_wait_sleep(&bars->kv_empty[st], ((i / kStages) + 1) & 1, p.err,
+                                     kRoleProducer | kBarKvEmpty | (unsigned)(i & 0xffff))) {
                     bars->abort = 1;
                     break;
                 }
@@ -256,7 +285,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 ++issued;
                 uint8_t* kt = smem + kOffKV + st * kStageBytes;
                 uint8_t* vt = kt + kTileBytes;
-                const int y = (int)(head_row0 + (int64_t)(t_begin + i) * kKeys);
+                const int64_t row0 = (i < n_hist) ? (int64_t)(t_begin + i) * kKeys : P;
+                const int y = (int)(head_row0 + row0);
                 mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
                 tma_load_2d(kt, &tmK, 0, y, &bars->kv_full[st]);
                 tma_load_2d(kt + kTileBytes / 2, &tmK, 64, y, &bars->kv_full[st]);
@@ -270,119 +300,170 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                               kRoleProducer | kBarKvFull | (unsigned)(i & 0xffff));
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ----------------------------
+        // Issues S_j = Q K_j^T and O_g += P_i V_i in the order their inputs
+        // become ready: S_j needs K/V tile j and the S buffer of group j & 1
+        // (free once P of tile j - 2 was handed over, i.e. j <= next_pv + 1);
+        // PV_i needs P of tile i.
         if (lane == 0) {
             const uint32_t qaddr = smem_base + kOffQ;
-            const uint32_t paddr = smem_base + kOffP;
-            auto issue_s = [&](int i) -> bool {
-                const int st = i % kStages;
-                if (!mbar_wait(&bars->kv_full[st], (i / kStages) & 1, p.err,
-                               kRoleMma | kBarKvFull | (unsigned)(i & 0xffff)))
-                    return false;
-                tc_fence_after();
-                const uint32_t kaddr = smem_base + kOffKV + st * kStageBytes;
-                const uint32_t dS = tmem + kTmemS + (uint32_t)((i & 1) * kKeys);
+            int next_s = 0, next_pv = 0;
+            bool ok = true;
+            uint64_t t_last = global_timer_ns();
+            while (next_pv < n) {
+                bool progressed = false;
+                if (next_s < n && next_s <= next_pv + 1 &&
+                    mbar_try_wait(&bars->kv_full[next_s % kStages], (next_s / kStages) & 1)) {
+                    tc_fence_after();
+                    const int j = next_s;
+                    const uint32_t kaddr = smem_base + kOffKV + (j % kStages) * kStageBytes;
+                    const uint32_t dS = tmem + kTmemS + (uint32_t)((j & 1) * kKeys);
 #pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t off = (uint32_t)((k >> 2) * (128 * 128) + (k & 3) * 32);
-                    const uint32_t koff = (uint32_t)((k >> 2) * (kKeys * 128) + (k & 3) * 32);
-                    mma_bf16(dS, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + koff, 16, 1024),
-                             kIdescS, k > 0 ? 1u : 0u);
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint32_t off = (uint32_t)((k >> 2) * (128 * 128) + (k & 3) * 32);
+                        const uint32_t koff = (uint32_t)((k >> 2) * (kKeys * 128) + (k & 3) * 32);
+                        mma_bf16(dS, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + koff, 16, 1024),
+                                 kIdescS, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars->s_full[j & 1]);
+                    ++next_s;
+                    progressed = true;
                 }
-                mma_commit(&bars->s_full[i & 1]);
-                return true;
-            };
-            bool ok = issue_s(0);
-            for (int i = 0; ok && i < n; ++i) {
-                if (i + 1 < n && !issue_s(i + 1)) { ok = false; break; }
-                if (!mbar_wait(&bars->p_full, i & 1, p.err,
-                               kRoleMma | kBarPFull | (unsigned)(i & 0xffff))) {
+                if (next_pv < next_s &&
+                    mbar_try_wait(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                    tc_fence_after();
+                    const int i = next_pv;
+                    const int gr = i & 1;
+                    const int st = i % kStages;
+                    const uint32_t paddr = smem_base + kOffP + gr * kPBytes;
+                    const uint32_t vaddr = smem_base + kOffKV + st * kStageBytes + kTileBytes;
+                    const uint32_t dO = tmem + kTmemO + (uint32_t)(gr * kD);
+#pragma unroll
+                    for (int k = 0; k < kKeys / 16; ++k) {
+                        mma_bf16(dO, sdesc(paddr + k * 32, 16, 1024),
+                                 sdesc(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
+                                 (i > 1 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars->p_free[gr]);
+                    mma_commit(&bars->kv_empty[st]);
+                    ++next_pv;
+                    progressed = true;
+                }
+                if (progressed) {
+                    t_last = global_timer_ns();
+                } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
+                    __nanosleep(32);   // leave the issue slots to the softmax warps
+                } else {
+                    atomicOr(p.err, kErrWaitTimeout);
+                    atomicCAS(p.err + 1, 0u,
+                              0x80000000u | kRoleMma | kBarPFull | (unsigned)(next_pv & 0xffff));
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const int st = i % kStages;
-                const uint32_t vaddr = smem_base + kOffKV + st * kStageBytes + kTileBytes;
-#pragma unroll
-                for (int k = 0; k < kKeys / 16; ++k) {
-                    mma_bf16(tmem + kTmemO, sdesc(paddr + k * 32, 16, 1024),
-                             sdesc(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
-                             (i > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(&bars->p_free);
-                mma_commit(&bars->kv_empty[st]);
             }
             if (!ok) bars->abort = 1;
             // drain: every MMA issued so far has completed once this arrives
             mma_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, p.err, kRoleMma | kBarDrain);
+            mbar_wait_sleep(&bars->drain, 0, p.err, kRoleMma | kBarDrain);
         }
     } else {
         // ------------------------------ softmax warps -------------------------
-        const int r = tid;                                    // query row = TMEM lane
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        // Group gr = warp / 4 takes tiles gr, gr + 2, ...; warp w owns TMEM
+        // lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.
+        const int q4 = warp & 3;
+        const int gr = warp >> 2;
+        const int r = q4 * 32 + lane;                         // query row = TMEM lane
+        const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t s_col = kTmemS + (uint32_t)(gr * kKeys);
+        const uint32_t o_col = kTmemO + (uint32_t)(gr * kD);
         const float c = p.scale_log2;
         const int64_t key_end = ((int64_t)t_end * kKeys < P) ? (int64_t)t_end * kKeys : P;
+        // visibility of the n_q speculative keys for this row (the masked tile)
+        uint64_t spec_bits = 0;
+        if (spec_here && ((n - 1) & 1) == gr && r < p.R) {
+            const int iq = r % p.n_q;
+            for (int j = 0; j < p.n_q; ++j) {
+                const bool vis =
+                    p.mask ? (p.mask[((int64_t)b * p.n_q + iq) * p.n_q + j] != 0) : (j <= iq);
+                spec_bits |= (vis ? 1ull : 0ull) << j;
+            }
+        }
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int i = 0; i < n; ++i) {
-            const bool got_s = mbar_wait(&bars->s_full[i & 1], (i >> 1) & 1, p.err,
-                                         kRoleSoftmax | kBarSFull | (unsigned)(i & 0xffff));
-            if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
+        int k_local = 0;
+        for (int i = gr; i < n; i += 2, ++k_local) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_sleep(&bars->s_full[gr], k_local & 1, p.err,
+                                            kRoleSoftmax | kBarSFull | (unsigned)(i & 0xffff)));
+            if (!ok) break;
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(lane_addr + kTmemS + (uint32_t)((i & 1) * kKeys), sr[0]);
-            tmem_ld32(lane_addr + kTmemS + (uint32_t)((i & 1) * kKeys) + 32, sr[1]);
+            tmem_ld32(lane_addr + s_col, sr[0]);
+            tmem_ld32(lane_addr + s_col + 32, sr[1]);
             tmem_wait_ld();
-            const int64_t key0 = (int64_t)(t_begin + i) * kKeys;
-            const int nvalid = (key_end - key0 < kKeys) ? (int)(key_end - key0) : kKeys;
-            float sv[64];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const float x = (j < nvalid) ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
-                sv[j] = x;
-                mx = fmaxf(mx, x);
+            uint64_t valid;
+            if (i < n_hist) {
+                const int64_t nv = key_end - (int64_t)(t_begin + i) * kKeys;
+                valid = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+            } else {
+                valid = spec_bits;
             }
-            const float mt = mx * c;
+            float sv[64];
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    sv[j + u] = ((valid >> (j + u)) & 1ull) ? __uint_as_float(sr[(j + u) >> 5][(j + u) & 31])
+                                                           : -INFINITY;
+                mx0 = fmaxf(mx0, sv[j]);
+                mx1 = fmaxf(mx1, sv[j + 1]);
+                mx2 = fmaxf(mx2, sv[j + 2]);
+                mx3 = fmaxf(mx3, sv[j + 3]);
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
             float corr = 1.f;
             bool rescale = false;
-            if (mt > m_run + 8.f) {               // also true for the first tile
-                corr = exp2f(m_run - mt);         // 0 when m_run = -inf
-                rescale = (i > 0);
+            if (mt > m_run + 8.f) {               // also true for the first finite tile
+                corr = ex2(m_run - mt);           // 0 when m_run = -inf
+                rescale = (k_local > 0);
                 m_run = mt;
             }
-            float sum = 0.f;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
             uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = exp2f(fmaf(sv[2 * j], c, -m_run));
-                const float p1 = exp2f(fmaf(sv[2 * j + 1], c, -m_run));
-                sum += p0 + p1;
+            for (int j = 0; j < 32; j += 2) {
+                const float p0 = ex2(fmaf(sv[2 * j], c, -m_run));
+                const float p1 = ex2(fmaf(sv[2 * j + 1], c, -m_run));
+                const float p2 = ex2(fmaf(sv[2 * j + 2], c, -m_run));
+                const float p3 = ex2(fmaf(sv[2 * j + 3], c, -m_run));
+                s0 += p0; s1 += p1; s2 += p2; s3 += p3;
                 pk[j] = pack_bf16x2(p0, p1);
+                pk[j + 1] = pack_bf16x2(p2, p3);
             }
-            l_run = l_run * corr + sum;
-            // PV of the previous tile must be done: it reads the P buffer and
-            // accumulates into O.
-            const bool got_free =
-                (i == 0) || mbar_wait(&bars->p_free, (i - 1) & 1, p.err,
-                                      kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff));
-            if (!__all_sync(0xffffffffu, got_free)) { ok = false; break; }
-            tc_fence_after();
+            l_run = l_run * corr + ((s0 + s1) + (s2 + s3));
+            // the previous PV of this group read P and accumulated into O
+            if (k_local > 0) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
+                                                kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff)));
+                if (!ok) break;
+                tc_fence_after();
+            }
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int q = 0; q < kD / 32; ++q) {
+                for (int qq = 0; qq < kD / 32; ++qq) {
                     uint32_t o[32];
-                    tmem_ld32(lane_addr + kTmemO + q * 32, o);
+                    tmem_ld32(lane_addr + o_col + qq * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
-                    tmem_st32(lane_addr + kTmemO + q * 32, o);
+                    tmem_st32(lane_addr + o_col + qq * 32, o);
                 }
                 tmem_wait_st();
             }
-            uint8_t* prow = smem + kOffP + r * 128;
+            uint8_t* prow = smem + kOffP + gr * kPBytes + r * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
@@ -390,41 +471,45 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars->p_full);
+            mbar_arrive(&bars->p_full[gr]);
         }
-        const bool got_last = ok && mbar_wait(&bars->p_free, (n - 1) & 1, p.err,
-                                              kRoleSoftmax | kBarPFree | 0xffffu);
-        if (__all_sync(0xffffffffu, got_last)) {
-            tc_fence_after();
-            // tcgen05.ld is warp-collective (.sync.aligned): every lane of the
-            // warp executes the same load instruction; only the stores depend
-            // on whether this lane's row is a real query row.
-            const bool real_row = r < p.R;
-            float* dst = p.part_acc + (slot + r) * kD;
+        if (tid == 0) griddep_launch_dependents();
+        // epilogue of a group that had tiles: its last PV, then the partial
+        if (ok && k_local > 0) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
+                                            kRoleSoftmax | kBarPFree | 0xffffu));
+            if (ok) {
+                tc_fence_after();
+                // tcgen05.ld is warp-collective (.sync.aligned): every lane
+                // executes the same loads; only the stores are per-row.
+                const bool real_row = r < p.R;
+                const int64_t row_slot = slot0 + gr * p.R + r;
+                float* dst = p.part_acc + row_slot * kD;
 #pragma unroll
-            for (int q = 0; q < kD / 32; ++q) {
-                uint32_t o[32];
-                tmem_ld32(lane_addr + kTmemO + q * 32, o);
-                tmem_wait_ld();
+                for (int qq = 0; qq < kD / 32; ++qq) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + o_col + qq * 32, o);
+                    tmem_wait_ld();
+                    if (real_row) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4*>(dst + qq * 32 + j) =
+                                make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
+                                            __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                    }
+                }
                 if (real_row) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(dst + q * 32 + j) =
-                            make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
-                                        __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                    p.part_ml[row_slot * 2 + 0] = m_run;
+                    p.part_ml[row_slot * 2 + 1] = l_run;
                 }
             }
-            if (real_row) {
-                p.part_ml[(slot + r) * 2 + 0] = m_run;
-                p.part_ml[(slot + r) * 2 + 1] = l_run;
-            }
-        } else {
-            bars->abort = 1;
         }
+        if (!ok) bars->abort = 1;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
@@ -476,9 +561,17 @@ cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.S, p.B * p.Hkv);
-    attn_prefix_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tmK, tmV, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.S, p.B * p.Hkv, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_prefix_tc_kernel, tmK, tmV, p);
 }
 
 }  // namespace rapid

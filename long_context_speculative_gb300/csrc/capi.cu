@@ -41,6 +41,7 @@ int sm_count() {
 struct AttnPlan {
     bool tc;        // tensor-core history kernel
     int S;          // splits of the history per (b, kv head)
+    int nparts;     // partial slots per (b, kv head)
     int64_t chunk;  // history rows per split
     size_t ws_bytes;
 };
@@ -68,9 +69,9 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     const int sms = sm_count();
     int64_t chunk;
     if (pl.tc) {
-        // One CTA per SM: spread B * Hkv heads over all SMs.
+        // One CTA per SM, one wave: spread B * Hkv heads over the SMs.
         const int64_t heads = (int64_t)B * Hkv;
-        int64_t S = (sms + heads - 1) / heads;
+        int64_t S = sms / heads;
         if (S < 1) S = 1;
         chunk = (max_prefix + S - 1) / S;
     } else {
@@ -84,9 +85,15 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     if (chunk < 128) chunk = 128;
     int64_t S = (max_prefix + chunk - 1) / chunk;
     if (S < 1) S = 1;
+    if (S > 512) {   // the merge kernel stages at most 1024 partial weights per row
+        S = 512;
+        chunk = ((max_prefix + S - 1) / S + 127) / 128 * 128;
+        S = (max_prefix + chunk - 1) / chunk;
+    }
     pl.S = (int)S;
     pl.chunk = chunk;
-    const size_t part = (size_t)B * Hkv * S * R;
+    pl.nparts = pl.tc ? 2 * (int)S : (int)S;   // two consumer groups per tensor-core CTA
+    const size_t part = (size_t)B * Hkv * pl.nparts * R;
     pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float));
     return pl;
 }
@@ -124,10 +131,12 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
     p.cap = kv_capacity; p.chunk = pl.chunk;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.n_q = n_q; p.G = Hq / Hkv; p.R = p.G * n_q;
     p.S = pl.S;
+    p.spec_in_partials = pl.tc ? 1 : 0;
+    p.nparts = pl.nparts;
     p.err = device_error_word();
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)d);
     p.scale_log2 = p.scale * kLog2e;
-    const size_t part = (size_t)B * Hkv * pl.S * p.R;
+    const size_t part = (size_t)B * Hkv * pl.nparts * p.R;
     p.part_acc = static_cast<float*>(workspace);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(part * d * sizeof(float)));

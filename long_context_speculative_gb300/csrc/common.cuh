@@ -72,6 +72,18 @@ RAPID_DEVICE Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32
 RAPID_DEVICE float word_uniform(uint32_t w) { return (float)(w >> 8) * (1.0f / 16777216.0f); }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while its predecessor in the stream is finishing;
+// griddep_wait() blocks until that predecessor has completed and its memory
+// is visible, so every kernel calls it before its first read of an input.
+// griddep_launch_dependents() lets the next kernel be scheduled early.
+// ---------------------------------------------------------------------------
+RAPID_DEVICE void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+RAPID_DEVICE void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // mbarrier + bulk-copy (TMA) primitives, inline PTX.
 // ---------------------------------------------------------------------------
 RAPID_DEVICE uint32_t smem_u32(const void* p) {
@@ -135,6 +147,37 @@ RAPID_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) break;
+    }
+    if (err) {
+        atomicOr(err, kErrWaitTimeout);
+        atomicCAS(err + 1, 0u, code | 0x80000000u);
+    }
+    return false;
+}
+
+// Blocking test of phase `parity` that suspends the thread for at most
+// `hint_ns` (mbarrier.try_wait with an explicit suspend-time hint), so a
+// waiting warp does not spin on issue slots.
+RAPID_DEVICE bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait like mbar_wait, but sleeping between polls.
+RAPID_DEVICE bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                  unsigned int code = 0, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (global_timer_ns() - t0 > limit_ns) break;
     }
     if (err) {
