@@ -176,121 +176,136 @@ attn_prefix_simt_kernel(const AttnParams p) {
     }
 }
 
-// One warp per query row (b, h, i), 8 rows per CTA: masked attention over the
-// n_q speculative rows, then the log-sum-exp merge with the S history partials:
+// One CTA of 128 threads per query row (b, h, i): the log-sum-exp merge of
+// the history partials (and, when the history kernel did not cover them, the
+// masked attention over the n_q speculative rows):
 //   M = max(m_spec, m_s);  L = sum_parts l_part 2^(m_part - M);
 //   O = sum_parts acc_part 2^(m_part - M) / L;   LSE = (M + log2 L) ln 2.
-// Latency-tolerant: the S (m, l) pairs are read in one coalesced sweep, the
-// split weights go through shared memory, and the partial rows are loaded
-// with independent, unrolled loads.
-constexpr int kMergeRows = 8;
+// Warps split the partials (s = warp, warp + 4, ...), lanes split the d
+// columns, so every load of a partial row is independent of the others.
+constexpr int kMergeThreads = 128;
 constexpr int kMergeMaxS = 1024;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(256) attn_merge_kernel(const AttnParams p) {
-    constexpr int NC = D / 32;
-    __shared__ float s_w[kMergeRows][kMergeMaxS + 64];   // split weights, then spec scores
+__global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
+    constexpr int VPL = D / 32;                 // columns per lane
+    __shared__ float s_w[kMergeMaxS];           // partial weights 2^(m_s - M)
+    __shared__ float s_red[4][D];
+    __shared__ float s_scal[4][2];
+    __shared__ float s_spec[2];                 // m_spec, l_spec (relative to m_spec)
     griddep_wait();
     griddep_launch_dependents();
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * kMergeRows + warp;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r = blockIdx.x;
     const int bg = blockIdx.y;
-    if (r >= p.R) return;
     const int b = bg / p.Hkv;
     const int g = bg % p.Hkv;
     const int h = g * p.G + r / p.n_q;
     const int i = r % p.n_q;
-    const int64_t P = clamped_prefix(p, b);
-    float* wsm = s_w[warp];
-    float* ssc = s_w[warp] + kMergeMaxS;
-
-    const T* Qrow = static_cast<const T*>(p.Q) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
-    const T* Kh = static_cast<const T*>(p.K) + (int64_t)bg * p.cap * D;
-    const T* Vh = static_cast<const T*>(p.V) + (int64_t)bg * p.cap * D;
-
-    // ---- speculative rows: scores (log2 domain) of the visible ones --------
-    // (skipped when the history kernel already folded them into a partial)
-    const int n_spec = p.spec_in_partials ? 0 : p.n_q;
-    float q[NC];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) q[c] = to_float(Qrow[lane + 32 * c]) * p.scale_log2;
-    float m_spec = -INFINITY;
-    for (int j = 0; j < n_spec; ++j) {
-        const bool vis = p.mask ? (p.mask[((int64_t)b * p.n_q + i) * p.n_q + j] != 0) : (j <= i);
-        float dot = 0.f;
-        if (vis) {
-            const T* kr = Kh + (P + j) * D;
-#pragma unroll
-            for (int c = 0; c < NC; ++c) dot = fmaf(q[c], to_float(kr[lane + 32 * c]), dot);
-        }
-        const float sj = vis ? warp_sum(dot) : -INFINITY;   // vis is warp-uniform
-        if (lane == 0) ssc[j] = sj;
-        m_spec = fmaxf(m_spec, sj);
-    }
-    // ---- history splits: (m, l) in one sweep --------------------------------
     const int nparts = p.nparts;
-    const float* ml = p.part_ml + ((int64_t)bg * nparts) * p.R * 2;
-    float M = m_spec;
-    for (int s0 = lane; s0 < nparts; s0 += 32) {
-        const float ls = ml[((int64_t)s0 * p.R + r) * 2 + 1];
-        const float ms = ml[((int64_t)s0 * p.R + r) * 2];
-        if (ls > 0.f) M = fmaxf(M, ms);
-    }
-    M = warp_max(M);
-    float Lpart = 0.f;
-    for (int s0 = lane; s0 < nparts; s0 += 32) {
-        const float ls = ml[((int64_t)s0 * p.R + r) * 2 + 1];
-        const float ms = ml[((int64_t)s0 * p.R + r) * 2];
-        const float w = ls > 0.f ? exp2f(ms - M) : 0.f;
-        wsm[s0] = w;
-        Lpart = fmaf(ls, w, Lpart);
-    }
-    float L = warp_sum(Lpart);
-    __syncwarp();
-    float acc[NC];
+    const float* ml = p.part_ml + ((int64_t)bg * nparts * p.R + r) * 2;     // + s * R * 2
+    const float* pa = p.part_acc + ((int64_t)bg * nparts * p.R + r) * D;    // + s * R * D
+    const int64_t mls = (int64_t)p.R * 2, pas = (int64_t)p.R * D;
+
+    // ---- speculative rows (warp 0), only when the history kernel skipped them
+    float acc_spec[VPL];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) acc[c] = 0.f;
-    // speculative V rows
-    for (int j = 0; j < n_spec; ++j) {
-        const float sj = ssc[j];
-        if (sj == -INFINITY) continue;                        // warp-uniform
-        const float w = exp2f(sj - M);
-        L += w;
-        const T* vr = Vh + (P + j) * D;
+    for (int c = 0; c < VPL; ++c) acc_spec[c] = 0.f;
+    float m_spec = -INFINITY;
+    if (warp == 0) {
+        float l_spec = 0.f;
+        if (!p.spec_in_partials) {
+            const int64_t P = clamped_prefix(p, b);
+            const T* Qrow = static_cast<const T*>(p.Q) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
+            const T* Kh = static_cast<const T*>(p.K) + (int64_t)bg * p.cap * D;
+            const T* Vh = static_cast<const T*>(p.V) + (int64_t)bg * p.cap * D;
+            float q[VPL];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, to_float(vr[lane + 32 * c]), acc[c]);
+            for (int c = 0; c < VPL; ++c) q[c] = to_float(Qrow[lane * VPL + c]) * p.scale_log2;
+            for (int j = 0; j < p.n_q; ++j) {
+                const bool vis =
+                    p.mask ? (p.mask[((int64_t)b * p.n_q + i) * p.n_q + j] != 0) : (j <= i);
+                if (!vis) continue;                                   // warp-uniform
+                const T* kr = Kh + (P + j) * D + lane * VPL;
+                const T* vr = Vh + (P + j) * D + lane * VPL;
+                float dot = 0.f;
+#pragma unroll
+                for (int c = 0; c < VPL; ++c) dot = fmaf(q[c], to_float(kr[c]), dot);
+                const float sj = warp_sum(dot);
+                const float mnew = fmaxf(m_spec, sj);
+                const float corr = exp2f(m_spec - mnew);
+                const float pj = exp2f(sj - mnew);
+                l_spec = l_spec * corr + pj;
+#pragma unroll
+                for (int c = 0; c < VPL; ++c) acc_spec[c] = fmaf(pj, to_float(vr[c]), acc_spec[c] * corr);
+                m_spec = mnew;
+            }
+        }
+        if (lane == 0) { s_spec[0] = m_spec; s_spec[1] = l_spec; }
     }
-    // history partials
-    const float* pa = p.part_acc + ((int64_t)bg * nparts) * p.R * D + (int64_t)r * D + lane;
-    const int64_t sstride = (int64_t)p.R * D;
-    int s0 = 0;
-    for (; s0 + 4 <= nparts; s0 += 4) {
-        float v[4][NC];
+    // ---- M over the history partials -------------------------------------
+    float mloc = -INFINITY;
+    for (int s = tid; s < nparts; s += kMergeThreads) {
+        if (ml[s * mls + 1] > 0.f) mloc = fmaxf(mloc, ml[s * mls]);
+    }
+    mloc = warp_max(mloc);
+    if (lane == 0) s_scal[warp][0] = mloc;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(fmaxf(s_scal[0][0], s_scal[1][0]), fmaxf(s_scal[2][0], s_scal[3][0])),
+                          s_spec[0]);
+    // ---- weights and L ---------------------------------------------------
+    float lloc = 0.f;
+    for (int s = tid; s < nparts; s += kMergeThreads) {
+        const float ls = ml[s * mls + 1];
+        const float w = ls > 0.f ? exp2f(ml[s * mls] - M) : 0.f;
+        s_w[s] = w;
+        lloc = fmaf(w, ls, lloc);
+    }
+    lloc = warp_sum(lloc);
+    if (lane == 0) s_scal[warp][1] = lloc;
+    __syncthreads();
+    const float wspec = (s_spec[1] > 0.f) ? exp2f(s_spec[0] - M) : 0.f;
+    const float L = (s_scal[0][1] + s_scal[1][1]) + (s_scal[2][1] + s_scal[3][1]) + wspec * s_spec[1];
+    // ---- weighted partial rows ---------------------------------------------
+    float acc[VPL];
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) acc[c] = 0.f;
+    int s = warp;
+    for (; s + 12 < nparts; s += 16) {
+        float v[4][VPL];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int c = 0; c < NC; ++c) v[u][c] = pa[(s0 + u) * sstride + 32 * c];
+            for (int c = 0; c < VPL; ++c) v[u][c] = pa[(s + 4 * u) * pas + lane * VPL + c];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const float w = wsm[s0 + u];
+            const float w = s_w[s + 4 * u];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, w != 0.f ? v[u][c] : 0.f, acc[c]);
+            for (int c = 0; c < VPL; ++c) acc[c] = fmaf(w, w != 0.f ? v[u][c] : 0.f, acc[c]);
         }
     }
-    for (; s0 < nparts; ++s0) {
-        const float w = wsm[s0];
+    for (; s < nparts; s += 4) {
+        const float w = s_w[s];
         if (w == 0.f) continue;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, pa[s0 * sstride + 32 * c], acc[c]);
+        for (int c = 0; c < VPL; ++c) acc[c] = fmaf(w, pa[s * pas + lane * VPL + c], acc[c]);
     }
-
-    T* Orow = static_cast<T*>(p.O) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-    for (int c = 0; c < NC; ++c) Orow[lane + 32 * c] = from_float<T>(acc[c] * inv);
-    if (lane == 0)
-        p.LSE[((int64_t)b * p.Hq + h) * p.n_q + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    for (int c = 0; c < VPL; ++c) s_red[warp][lane * VPL + c] = acc[c];
+    __syncthreads();
+    if (warp == 0) {
+        T* Orow = static_cast<T*>(p.O) + (((int64_t)b * p.Hq + h) * p.n_q + i) * D;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) {
+            const int col = lane * VPL + c;
+            const float o = (s_red[0][col] + s_red[1][col]) + (s_red[2][col] + s_red[3][col]) +
+                            wspec * acc_spec[c];
+            Orow[col] = from_float<T>(o * inv);
+        }
+        if (lane == 0)
+            p.LSE[((int64_t)b * p.Hq + h) * p.n_q + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
 }
 
 template <typename T, int D>
@@ -308,8 +323,8 @@ template <typename T, int D>
 cudaError_t launch_merge_typed(const AttnParams& p, cudaStream_t st) {
     if (p.nparts > kMergeMaxS) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.R + kMergeRows - 1) / kMergeRows, p.B * p.Hkv, 1);
-    cfg.blockDim = dim3(32 * kMergeRows, 1, 1);
+    cfg.gridDim = dim3(p.R, p.B * p.Hkv, 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -15,9 +15,9 @@
 //              lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.  A
 //              group turns its S tile into P (bf16, its own shared buffer),
 //              keeps its running max / sum and rescales its O in TMEM when the
-//              max grows by more than 2^8.  Each group leaves its own partial
-//              (the merge combines them like any other split).
-//   warp 8     TMA producer: 64-key K and V tiles into a 4-stage ring; the
+//              max grows by more than 2^8.  At the end the two groups combine
+//              their (O, m, l) into the split's one partial.
+//   warp 8     TMA producer: 64-key K and V tiles into a 5-stage ring; the
 //              last split also loads the n_q speculative rows as one more
 //              tile, which the softmax masks with the chain / tree mask.
 //   warp 9     allocates TMEM and issues the MMAs (one thread), in the order
@@ -44,7 +44,7 @@ constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kD = 128;
 constexpr int kKeys = 64;                       // keys per K/V tile
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr uint32_t kTmemCols = 512;   // S of group 0/1: [0,64) [64,128); O of group 0/1: [128,256) [256,384)
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 128;
@@ -173,6 +173,7 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
+    int grp_ok[2];        // cleared by a group that failed a wait
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block too small");
 
@@ -205,6 +206,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
+        bars->grp_ok[0] = 1;
+        bars->grp_ok[1] = 1;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -227,7 +230,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int n_hist = t_end - t_begin;
     const bool spec_here = (s == p.S - 1);
     const int n = n_hist + (spec_here ? 1 : 0);
-    const int64_t slot0 = ((int64_t)bg * p.nparts + 2 * s) * p.R;   // group g: slot0 + g * R
+    const int64_t slot = ((int64_t)bg * p.nparts + s) * p.R;
 
     // Q rows of the group into shared memory (K-major, 128-byte swizzle);
     // rows >= R are zero.
@@ -252,13 +255,9 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
         fence_proxy_async_smem();
     }
-    // A group without tiles leaves an empty partial: m = -inf, l = 0.
-    if (tid < 2 * 128) {
-        const int gr = tid >> 7, r = tid & 127;
-        if (gr >= n && r < p.R) {
-            p.part_ml[(slot0 + gr * p.R + r) * 2 + 0] = -INFINITY;
-            p.part_ml[(slot0 + gr * p.R + r) * 2 + 1] = 0.f;
-        }
+    if (n <= 0 && tid < p.R) {   // empty split: m = -inf, l = 0 (no tile touched)
+        p.part_ml[(slot + tid) * 2 + 0] = -INFINITY;
+        p.part_ml[(slot + tid) * 2 + 1] = 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -474,35 +473,58 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mbar_arrive(&bars->p_full[gr]);
         }
         if (tid == 0) griddep_launch_dependents();
-        // epilogue of a group that had tiles: its last PV, then the partial
-        if (ok && k_local > 0) {
+        // Wait for this group's last PV, publish (m, l), then combine both
+        // groups' O columns: warp w writes columns 64 (w / 4) .. + 63 of its rows.
+        if (ok && k_local > 0)
             ok = __all_sync(0xffffffffu,
                             mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
                                             kRoleSoftmax | kBarPFree | 0xffffu));
-            if (ok) {
-                tc_fence_after();
-                // tcgen05.ld is warp-collective (.sync.aligned): every lane
-                // executes the same loads; only the stores are per-row.
-                const bool real_row = r < p.R;
-                const int64_t row_slot = slot0 + gr * p.R + r;
-                float* dst = p.part_acc + row_slot * kD;
+        // (m, l) of this group go into its own P buffer, which its last PV
+        // product has finished reading.
+        float* pub = reinterpret_cast<float*>(smem + kOffP + gr * kPBytes);
+        if (ok) {
+            pub[r] = k_local > 0 ? m_run : -INFINITY;
+            pub[128 + r] = k_local > 0 ? l_run : 0.f;
+        }
+        if (!ok && lane == 0) bars->grp_ok[gr] = 0;   // any warp of the group can veto
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        ok = bars->grp_ok[0] && bars->grp_ok[1];
+        if (ok) {
+            tc_fence_after();
+            const float* pub0 = reinterpret_cast<const float*>(smem + kOffP);
+            const float* pub1 = reinterpret_cast<const float*>(smem + kOffP + kPBytes);
+            const float m0 = pub0[r], m1 = pub1[r];
+            const float l0 = pub0[128 + r], l1 = pub1[128 + r];
+            const float M = fmaxf(m0, m1);
+            const bool has0 = l0 > 0.f, has1 = l1 > 0.f;
+            const float w0 = has0 ? ex2(m0 - M) : 0.f;
+            const float w1 = has1 ? ex2(m1 - M) : 0.f;
+            // tcgen05.ld is warp-collective (.sync.aligned): every lane
+            // executes the same loads; only the stores are per-row.
+            const bool real_row = r < p.R;
+            const int half = gr;                      // this warp's 64 output columns
+            float* dst = p.part_acc + (slot + r) * kD + half * 64;
 #pragma unroll
-                for (int qq = 0; qq < kD / 32; ++qq) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_addr + o_col + qq * 32, o);
-                    tmem_wait_ld();
-                    if (real_row) {
+            for (int qq = 0; qq < 2; ++qq) {
+                uint32_t o0[32], o1[32];
+                tmem_ld32(lane_addr + kTmemO + half * 64 + qq * 32, o0);
+                tmem_ld32(lane_addr + kTmemO + kD + half * 64 + qq * 32, o1);
+                tmem_wait_ld();
+                if (real_row) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4*>(dst + qq * 32 + j) =
-                                make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
-                                            __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                    for (int j = 0; j < 32; j += 4) {
+                        float4 v;
+                        v.x = (has0 ? w0 * __uint_as_float(o0[j]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[j]) : 0.f);
+                        v.y = (has0 ? w0 * __uint_as_float(o0[j + 1]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[j + 1]) : 0.f);
+                        v.z = (has0 ? w0 * __uint_as_float(o0[j + 2]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[j + 2]) : 0.f);
+                        v.w = (has0 ? w0 * __uint_as_float(o0[j + 3]) : 0.f) + (has1 ? w1 * __uint_as_float(o1[j + 3]) : 0.f);
+                        *reinterpret_cast<float4*>(dst + qq * 32 + j) = v;
                     }
                 }
-                if (real_row) {
-                    p.part_ml[row_slot * 2 + 0] = m_run;
-                    p.part_ml[row_slot * 2 + 1] = l_run;
-                }
+            }
+            if (real_row && half == 0) {
+                p.part_ml[(slot + r) * 2 + 0] = M;
+                p.part_ml[(slot + r) * 2 + 1] = l0 * w0 + l1 * w1;
             }
         }
         if (!ok) bars->abort = 1;

@@ -92,7 +92,7 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     }
     pl.S = (int)S;
     pl.chunk = chunk;
-    pl.nparts = pl.tc ? 2 * (int)S : (int)S;   // two consumer groups per tensor-core CTA
+    pl.nparts = (int)S;
     const size_t part = (size_t)B * Hkv * pl.nparts * R;
     pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float));
     return pl;
