@@ -104,19 +104,19 @@ def _peaks():
 
 
 def _traffic_for(kernel_key: str):
-    """ncu DRAM bytes per launch from profiles/traffic.json, if the kernel source
-    is unchanged since the capture (sha256 of its sources), else None."""
+    """ncu DRAM bytes per launch from profiles/traffic.txt, if the kernel
+    sources are unchanged since the capture (sha256 of its sources), else None."""
     try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            tr = json.load(f)
-        ent = tr[kernel_key]
-        h = hashlib.sha256()
-        for p in SRC_FILES_TRAFFIC:
-            with open(os.path.join(ROOT, p), "rb") as f:
-                h.update(f.read())
-        if ent.get("src_sha256") != h.hexdigest():
+        rec = {}
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            for line in f:
+                if line.startswith("#") or not line.strip():
+                    continue
+                k, v = line.split(None, 1)
+                rec[k] = v.strip()
+        if rec.get("key") != kernel_key or rec.get("src_sha256") != src_hash():
             return None
-        return ent["dram_bytes_per_launch"]
+        return int(rec["dram_bytes_per_launch"])
     except Exception:
         return None
 

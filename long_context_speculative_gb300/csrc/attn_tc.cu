@@ -9,7 +9,7 @@
 // group's G * n_q query rows form the M = 128 operand of one tcgen05 MMA, so
 // every K/V byte is read from HBM once per group.
 //
-// CTA = (split s, sequence b * Hkv + KV head g); 320 threads:
+// CTA = (split s, sequence b * Hkv + KV head g); 352 threads:
 //   warps 0-7  softmax, in two consumer groups (warps 0-3 take the even
 //              tiles of the split, warps 4-7 the odd ones); warp w owns TMEM
 //              lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.  A
@@ -17,11 +17,13 @@
 //              keeps its running max / sum and rescales its O in TMEM when the
 //              max grows by more than 2^8.  At the end the two groups combine
 //              their (O, m, l) into the split's one partial.
-//   warp 8     TMA producer: 64-key K and V tiles into a 5-stage ring; the
+//   warp 8     TMA producer: 64-key K and V tiles into a 6-stage ring (5 when
+//              the group has more than 64 query rows); the
 //              last split also loads the n_q speculative rows as one more
 //              tile, which the softmax masks with the chain / tree mask.
-//   warp 9     allocates TMEM and issues the MMAs (one thread), in the order
-//              their inputs become ready: S_j = Q K_j^T (M128 N64 K128) and
+//   warp 10    allocates TMEM and issues the MMAs (one thread), in the order
+//              their inputs become ready: S_j = Q K_j^T (M128 N64 K128, two S
+//              buffers per group, so S runs a tile ahead of the softmax) and
 //              O_g += P_i V_i (M128 N128 K64).
 // Shared-memory operands use the 128-byte swizzle; Q, K and P are K-major,
 // V is MN-major (d contiguous).  Every mbarrier wait is bounded in wall-clock
@@ -37,28 +39,43 @@ namespace rapid {
 
 namespace {
 
-constexpr int kSoftmaxWarps = 8;                // two per TMEM lane quadrant
-constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kSoftmaxWarps = 8;                // two groups x four TMEM lane quadrants
+// The producer runs on SM sub-partition 0 (warp 8); warp 9 is idle so that the
+// MMA issuer (warp 10) sits on sub-partition 2, away from the producer.
 constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kMmaWarp = kSoftmaxWarps + 2;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr int kD = 128;
 constexpr int kKeys = 64;                       // keys per K/V tile
-constexpr int kStages = 5;
-constexpr uint32_t kTmemCols = 512;   // S of group 0/1: [0,64) [64,128); O of group 0/1: [128,256) [256,384)
+constexpr int kMaxStages = 6;
+// TMEM columns: S of group g, buffer u at 64 (2 g + u); O of group g at 256 + 128 g.
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
-constexpr uint32_t kTmemO = 128;
-
-constexpr int kQBytes = 128 * kD * 2;           // 2 column blocks x 16 KB
-constexpr int kPBytes = 128 * kKeys * 2;        // 16 KB per P buffer (two buffers)
+constexpr uint32_t kTmemO = 256;
 constexpr int kTileBytes = kKeys * kD * 2;      // 16 KB: 2 column blocks x 8 KB
 constexpr int kStageBytes = 2 * kTileBytes;     // K + V
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;
 constexpr int kBarBytes = 256;
-constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + 1 KB alignment slack
+
+// Shared-memory plan for ROWS query rows kept on chip (64 when the group has
+// at most 64 rows, else 128).  The MMAs always run with M = 128: with ROWS =
+// 64 the operand rows 64..127 of Q and P read the neighbouring (finite)
+// shared data and only produce output rows that are never used, which frees
+// 32 KB for a sixth K/V stage.
+template <int ROWS>
+struct Plan {
+    static constexpr int kActiveQuadrants = ROWS / 32;   // softmax warps per group
+    static constexpr int kGroupThreads = 32 * kActiveQuadrants;
+    static constexpr int kStages = ROWS == 64 ? 6 : 5;
+    static constexpr int kQBlock = ROWS * 128;           // one 64-column block of Q
+    static constexpr int kPBytes = ROWS * 128;           // one P buffer (64 keys)
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffP = kOffQ + 2 * kQBlock;
+    static constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
+    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + 1 KB alignment slack
+    static_assert(kStages <= kMaxStages, "too many stages");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 // Instruction descriptors (kind::f16): D = f32 (bits 4-5 = 1), A = B = bf16
 // (bits 7-9 = 1, bits 10-12 = 1), bit 15/16 = A/B MN-major, bits 17-22 = N/8,
@@ -165,10 +182,10 @@ enum : unsigned int {
 };
 
 struct Bars {
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t s_full[2];   // S of consumer group g written
-    uint64_t p_full[2];   // P of group g written (kSoftmaxThreads / 2 arrivals)
+    uint64_t kv_full[kMaxStages];
+    uint64_t kv_empty[kMaxStages];
+    uint64_t s_full[4];   // S buffer u of consumer group g written: index 2 g + u
+    uint64_t p_full[2];   // P of group g written (one arrival per active softmax thread)
     uint64_t p_free[2];   // PV product of group g done
     uint64_t drain;
     uint32_t tmem_base;
@@ -177,9 +194,17 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block too small");
 
+template <int ROWS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using L = Plan<ROWS>;
+    constexpr int kStages = L::kStages;
+    constexpr int kOffQ = L::kOffQ;
+    constexpr int kOffP = L::kOffP;
+    constexpr int kOffKV = L::kOffKV;
+    constexpr int kOffBar = L::kOffBar;
+    constexpr int kPBytes = L::kPBytes;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window address (128-byte swizzle atoms).
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -199,9 +224,9 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mbar_init(&bars->kv_full[i], 1);
             mbar_init(&bars->kv_empty[i], 1);
         }
+        for (int u = 0; u < 4; ++u) mbar_init(&bars->s_full[u], 1);
         for (int gr = 0; gr < 2; ++gr) {
-            mbar_init(&bars->s_full[gr], 1);
-            mbar_init(&bars->p_full[gr], kSoftmaxThreads / 2);
+            mbar_init(&bars->p_full[gr], L::kGroupThreads);
             mbar_init(&bars->p_free[gr], 1);
         }
         mbar_init(&bars->drain, 1);
@@ -234,7 +259,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 
     // Q rows of the group into shared memory (K-major, 128-byte swizzle);
     // rows >= R are zero.
-    if (tid < 128 && n > 0) {
+    if (tid < ROWS && n > 0) {
         const int r = tid;
         uint4 chunk[16];
         if (r < p.R) {
@@ -250,7 +275,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int blk = j >> 3, jj = j & 7;
-            *reinterpret_cast<uint4*>(smem + kOffQ + blk * (128 * 128) + r * 128 +
+            *reinterpret_cast<uint4*>(smem + kOffQ + blk * L::kQBlock + r * 128 +
                                       ((jj ^ (r & 7)) << 4)) = chunk[j];
         }
         fence_proxy_async_smem();
@@ -271,6 +296,11 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     } else if (warp == kProducerWarp) {
         // ------------------------------ TMA producer --------------------------
         if (lane == 0) {
+            // Tile i's rows in the cache (the speculative tile starts at P).
+            auto tile_y = [&](int i) -> int {
+                const int64_t row0 = (i < n_hist) ? (int64_t)(t_begin + i) * kKeys : P;
+                return (int)(head_row0 + row0);
+            };
             int issued = 0;
             for (int i = 0; i < n; ++i) {
                 const int st = i % kStages;
@@ -284,8 +314,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 ++issued;
                 uint8_t* kt = smem + kOffKV + st * kStageBytes;
                 uint8_t* vt = kt + kTileBytes;
-                const int64_t row0 = (i < n_hist) ? (int64_t)(t_begin + i) * kKeys : P;
-                const int y = (int)(head_row0 + row0);
+                const int y = tile_y(i);
                 mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
                 tma_load_2d(kt, &tmK, 0, y, &bars->kv_full[st]);
                 tma_load_2d(kt + kTileBytes / 2, &tmK, 64, y, &bars->kv_full[st]);
@@ -302,30 +331,36 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ----------------------------
         // Issues S_j = Q K_j^T and O_g += P_i V_i in the order their inputs
-        // become ready: S_j needs K/V tile j and the S buffer of group j & 1
-        // (free once P of tile j - 2 was handed over, i.e. j <= next_pv + 1);
-        // PV_i needs P of tile i.
+        // become ready: S_j needs K/V tile j and its S buffer (group j & 1,
+        // buffer (j >> 1) & 1), which is free once P of tile j - 4 was handed
+        // over, i.e. j <= next_pv + 3; PV_i needs P of tile i.
         if (lane == 0) {
-            const uint32_t qaddr = smem_base + kOffQ;
+            // Descriptors are built once; the one of a later operand block is
+            // the base plus its byte offset in 16-byte units (all shared
+            // addresses stay below 256 KB, so the 14-bit field never carries).
+            const uint64_t qd0 = sdesc(smem_base + kOffQ, 16, 1024);
+            const uint64_t kd0 = sdesc(smem_base + kOffKV, 16, 1024);
+            const uint64_t pd0 = sdesc(smem_base + kOffP, 16, 1024);
+            const uint64_t vd0 = sdesc(smem_base + kOffKV + kTileBytes, kTileBytes / 2, 1024);
             int next_s = 0, next_pv = 0;
             bool ok = true;
             uint64_t t_last = global_timer_ns();
             while (next_pv < n) {
                 bool progressed = false;
-                if (next_s < n && next_s <= next_pv + 1 &&
+                if (next_s < n && next_s <= next_pv + 3 &&
                     mbar_try_wait(&bars->kv_full[next_s % kStages], (next_s / kStages) & 1)) {
                     tc_fence_after();
                     const int j = next_s;
-                    const uint32_t kaddr = smem_base + kOffKV + (j % kStages) * kStageBytes;
-                    const uint32_t dS = tmem + kTmemS + (uint32_t)((j & 1) * kKeys);
+                    const int sbuf = 2 * (j & 1) + ((j >> 1) & 1);
+                    const uint32_t dS = tmem + kTmemS + (uint32_t)(sbuf * kKeys);
+                    const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
-                        const uint32_t off = (uint32_t)((k >> 2) * (128 * 128) + (k & 3) * 32);
-                        const uint32_t koff = (uint32_t)((k >> 2) * (kKeys * 128) + (k & 3) * 32);
-                        mma_bf16(dS, sdesc(qaddr + off, 16, 1024), sdesc(kaddr + koff, 16, 1024),
-                                 kIdescS, k > 0 ? 1u : 0u);
+                        const uint64_t qoff = (uint64_t)(((k >> 2) * L::kQBlock + (k & 3) * 32) >> 4);
+                        const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
+                        mma_bf16(dS, qd0 + qoff, kd + koff, kIdescS, k > 0 ? 1u : 0u);
                     }
-                    mma_commit(&bars->s_full[j & 1]);
+                    mma_commit(&bars->s_full[sbuf]);
                     ++next_s;
                     progressed = true;
                 }
@@ -335,14 +370,13 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                     const int i = next_pv;
                     const int gr = i & 1;
                     const int st = i % kStages;
-                    const uint32_t paddr = smem_base + kOffP + gr * kPBytes;
-                    const uint32_t vaddr = smem_base + kOffKV + st * kStageBytes + kTileBytes;
+                    const uint64_t pd = pd0 + (uint64_t)(gr * (kPBytes >> 4));
+                    const uint64_t vd = vd0 + (uint64_t)(st * (kStageBytes >> 4));
                     const uint32_t dO = tmem + kTmemO + (uint32_t)(gr * kD);
 #pragma unroll
                     for (int k = 0; k < kKeys / 16; ++k) {
-                        mma_bf16(dO, sdesc(paddr + k * 32, 16, 1024),
-                                 sdesc(vaddr + k * 2048, kTileBytes / 2, 1024), kIdescPV,
-                                 (i > 1 || k > 0) ? 1u : 0u);
+                        mma_bf16(dO, pd + (uint64_t)(k * 2), vd + (uint64_t)(k * (2048 >> 4)),
+                                 kIdescPV, (i > 1 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(&bars->p_free[gr]);
                     mma_commit(&bars->kv_empty[st]);
@@ -352,7 +386,14 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 if (progressed) {
                     t_last = global_timer_ns();
                 } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
-                    __nanosleep(32);   // leave the issue slots to the softmax warps
+                    // Nothing ready: suspend on the barrier whose completion
+                    // unblocks the most (a pending PV first); the thread
+                    // wakes as soon as that phase completes.
+                    if (next_pv < next_s)
+                        (void)mbar_try_wait_sleep(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1, 500u);
+                    else if (next_s < n)
+                        (void)mbar_try_wait_sleep(&bars->kv_full[next_s % kStages],
+                                                  (next_s / kStages) & 1, 500u);
                 } else {
                     atomicOr(p.err, kErrWaitTimeout);
                     atomicCAS(p.err + 1, 0u,
@@ -366,7 +407,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mma_commit(&bars->drain);
             mbar_wait_sleep(&bars->drain, 0, p.err, kRoleMma | kBarDrain);
         }
-    } else {
+    } else if (warp < kSoftmaxWarps && (warp & 3) < L::kActiveQuadrants) {
         // ------------------------------ softmax warps -------------------------
         // Group gr = warp / 4 takes tiles gr, gr + 2, ...; warp w owns TMEM
         // lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.
@@ -374,7 +415,6 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         const int gr = warp >> 2;
         const int r = q4 * 32 + lane;                         // query row = TMEM lane
         const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
-        const uint32_t s_col = kTmemS + (uint32_t)(gr * kKeys);
         const uint32_t o_col = kTmemO + (uint32_t)(gr * kD);
         const float c = p.scale_log2;
         const int64_t key_end = ((int64_t)t_end * kKeys < P) ? (int64_t)t_end * kKeys : P;
@@ -392,8 +432,10 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         bool ok = true;
         int k_local = 0;
         for (int i = gr; i < n; i += 2, ++k_local) {
+            const int sbuf = 2 * gr + (k_local & 1);
+            const uint32_t s_col = kTmemS + (uint32_t)(sbuf * kKeys);
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_sleep(&bars->s_full[gr], k_local & 1, p.err,
+                            mbar_wait_sleep(&bars->s_full[sbuf], (k_local >> 1) & 1, p.err,
                                             kRoleSoftmax | kBarSFull | (unsigned)(i & 0xffff)));
             if (!ok) break;
             tc_fence_after();
@@ -487,7 +529,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             pub[128 + r] = k_local > 0 ? l_run : 0.f;
         }
         if (!ok && lane == 0) bars->grp_ok[gr] = 0;   // any warp of the group can veto
-        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(2 * L::kGroupThreads) : "memory");
         ok = bars->grp_ok[0] && bars->grp_ok[1];
         if (ok) {
             tc_fence_after();
@@ -575,25 +617,36 @@ bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
     return tensor_map_encoder() != nullptr;
 }
 
-cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
-    CUtensorMap tmK, tmV;
-    const uint64_t rows = (uint64_t)p.B * p.Hkv * p.cap;
-    if (!make_kv_map(&tmK, p.K, rows) || !make_kv_map(&tmV, p.V, rows))
-        return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(attn_prefix_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+namespace {
+
+template <int ROWS>
+cudaError_t launch_rows(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
+                        cudaStream_t st) {
+    auto kern = attn_prefix_tc_kernel<ROWS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Plan<ROWS>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.S, p.B * p.Hkv, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = Plan<ROWS>::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_prefix_tc_kernel, tmK, tmV, p);
+    return cudaLaunchKernelEx(&cfg, kern, tmK, tmV, p);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
+    CUtensorMap tmK, tmV;
+    const uint64_t rows = (uint64_t)p.B * p.Hkv * p.cap;
+    if (!make_kv_map(&tmK, p.K, rows) || !make_kv_map(&tmV, p.V, rows))
+        return cudaErrorInvalidValue;
+    return p.R <= 64 ? launch_rows<64>(tmK, tmV, p, st) : launch_rows<128>(tmK, tmV, p, st);
 }
 
 }  // namespace rapid
