@@ -183,6 +183,42 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft,
                           float* diag, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Largest B * n_q that rapid_accept_noalloc accepts. */
+enum { RAPID_NOALLOC_MAX_NODES = 4096 };
+
+/*
+ * rapid_accept without a workspace argument, for callers that cannot
+ * allocate device memory where they run the acceptance step: a host framework
+ * that owns all device memory and gives its plug-ins no allocator, or a
+ * latency-critical decode loop that must never call cudaMalloc (it may
+ * synchronise the device).  The pages have no counterpart of this entry
+ * point; it computes exactly what rapid_accept computes, with the same
+ * arguments and outputs.
+ *
+ * Scratch: a statically allocated device array of 32 KB inside librapid.so,
+ * held by every GPU that loads the library until the process exits.  It fits
+ * B * n_q <= RAPID_NOALLOC_MAX_NODES; larger sizes return RAPID_EUNSUPPORTED.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  Its first call on a device looks up the array's device address
+ * with cudaGetSymbolAddress while that device is current; make that first
+ * call before any stream capture.
+ *
+ * Concurrency: every call on a device shares the one array, and the array
+ * keeps the last call's contents.  Calls whose kernels overlap on the GPU
+ * (different streams, or different host threads, without ordering between
+ * them) race on it and give wrong results; order such calls, for example on
+ * one stream.
+ *
+ * Errors: those of rapid_accept, plus RAPID_EUNSUPPORTED for B * n_q over the
+ * limit and RAPID_ECUDA when the array's address cannot be obtained.
+ */
+rapid_status rapid_accept_noalloc(const float* z_target, const float* q_draft,
+                                  const int32_t* draft_tokens, const int32_t* parent,
+                                  int B, int n_q, int V, float T, float eta,
+                                  uint64_t philox_seed, uint32_t flags,
+                                  int32_t* n_accepted, int32_t* next_token, int32_t* path,
+                                  float* diag, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Misc                                                                      */
 /* ------------------------------------------------------------------------ */

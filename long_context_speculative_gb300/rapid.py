@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
     L.rapid_device_error.restype = i32
     L.rapid_device_error_info.argtypes = [vp, i32]
     L.rapid_device_error_info.restype = i32
+    L.rapid_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp,
+                                       vp, vp, vp]
+    L.rapid_accept_noalloc.restype = i32
     _lib = L
     return L
 
@@ -130,6 +133,19 @@ def rapid_accept(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, f
                             _ptr(diag), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "rapid_accept")
+
+
+def rapid_accept_noalloc(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, flags,
+                         n_accepted, next_token, path, diag, stream=None):
+    """rapid_accept with the library's static scratch instead of a workspace."""
+    _need_cuda(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag)
+    B, n_q, V = z_target.shape
+    st = lib().rapid_accept_noalloc(_ptr(z_target), _ptr(q_draft), _ptr(draft_tokens),
+                                    _ptr(parent), B, n_q, V, float(T), float(eta),
+                                    int(philox_seed) & ((1 << 64) - 1), int(flags),
+                                    _ptr(n_accepted), _ptr(next_token), _ptr(path), _ptr(diag),
+                                    _stream(stream))
+    _check(st, "rapid_accept_noalloc")
 
 
 def rapid_device_error(clear: bool = True) -> int:
