@@ -223,13 +223,18 @@ def run_gpu(args, w):
     # ---- resident inputs: one KV cache and one Q per layer ------------------
     cap = w.capacity
     Ks, Vs, Qs = [], [], []
+    mask = None
+    prefix_len = None
+    parents = None
     for layer in range(w.layers):
         a = wl.attn_inputs(w, layer=layer, device=dev)
         Ks.append(a.K); Vs.append(a.V); Qs.append(a.Q)
+        if layer == 0:
+            mask, prefix_len, parents = a.mask, a.prefix_len, a.parents
         del a
-    prefix_len = torch.full((w.B,), w.prefix, dtype=torch.int32, device=dev)
-    acc_in = wl.accept_inputs(w)
+    acc_in = wl.accept_inputs(w, parents=parents if w.tree else None)
     z = acc_in.z.to(dev); q = acc_in.q.to(dev); tok = acc_in.tokens.to(dev)
+    par = None if acc_in.parent is None else acc_in.parent.to(dev)
     Os = [torch.empty_like(Qs[0]) for _ in range(w.layers)]
     Ls = [torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
           for _ in range(w.layers)]
@@ -245,11 +250,11 @@ def run_gpu(args, w):
         for layer in range(w.layers):
             if ev is not None:
                 ev[layer].record(stream)
-            rapid.rapid_verify_attn(Qs[layer], Ks[layer], Vs[layer], prefix_len, None, 0.0,
+            rapid.rapid_verify_attn(Qs[layer], Ks[layer], Vs[layer], prefix_len, mask, 0.0,
                                     Os[layer], Ls[layer], ws_attn)
         if ev is not None:
             ev[w.layers].record(stream)
-        rapid.rapid_accept(z, q, tok, None, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
                            n_acc, nxt, None, None, ws_acc)
 
     for i in range(args.warmup):
@@ -301,9 +306,9 @@ def run_gpu(args, w):
         z.copy_(hz, non_blocking=True); q.copy_(hq, non_blocking=True)
         tok.copy_(htok, non_blocking=True)
         for layer in range(w.layers):
-            rapid.rapid_verify_attn(dQ[layer], Ks[layer], Vs[layer], prefix_len, None, 0.0,
+            rapid.rapid_verify_attn(dQ[layer], Ks[layer], Vs[layer], prefix_len, mask, 0.0,
                                     Os[layer], Ls[layer], ws_attn)
-        rapid.rapid_accept(z, q, tok, None, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
                            res_dev[:w.B], res_dev[w.B:], None, None, ws_acc)
         for layer in range(w.layers):
             hO[layer].copy_(Os[layer], non_blocking=True)
@@ -326,11 +331,15 @@ def run_gpu(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
+    # ---- acceptance bandwidth on a batch larger than L2 -----------------------
+    acc_roof = accept_batch_roofline(w, dev, stream)
+
     # ---- numbers -----------------------------------------------------------
     ms_per_step = total_ms / args.steps
     value = ws * args.steps / (total_ms / 1e3)
     e2e_value = ws * args.steps / (e2e_ms / 1e3)
-    kv_bytes = 2 * w.B * w.Hkv * (w.prefix + w.n_q) * w.d * 2
+    kv_rows = int(prefix_len.sum().item()) + w.B * w.n_q
+    kv_bytes = 2 * w.Hkv * kv_rows * w.d * 2
     qo_bytes = 2 * w.B * w.Hq * w.n_q * w.d * 2 + w.B * w.Hq * w.n_q * 4
     per_call = kv_bytes + qo_bytes
     attn_ms.sort()
@@ -355,6 +364,7 @@ def run_gpu(args, w):
                          "avg_launch_ms": avg_call_ms},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
+            "accept_roofline": acc_roof,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": wall}
@@ -369,6 +379,45 @@ def run_gpu(args, w):
         dist.destroy_process_group()
 
 
+def accept_batch_roofline(w, dev, stream, reps=20):
+    """rapid_accept alone on a batch of at least 100 MB of z + q (16 sequences of
+    the workload's chain shape, larger than L2): algorithmic bytes = 8 B per
+    vocabulary entry (z and q read once) / CUDA-event time per call."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    Bb = max(1, -(-100_000_000 // (w.n_q * w.V * 8)))
+    inp = wl.accept_inputs(w, B=Bb, parents=None if not w.tree else None)
+    z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
+    par = None if inp.parent is None else inp.parent.to(dev)
+    nbytes = z.numel() * 4 + q.numel() * 4
+    ws = torch.empty(rapid.rapid_accept_workspace_size(Bb, w.n_q, w.V), dtype=torch.uint8,
+                     device=dev)
+    na = torch.empty(Bb, dtype=torch.int32, device=dev)
+    nt = torch.empty(Bb, dtype=torch.int32, device=dev)
+    for i in range(3):
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, i, rapid.RAPID_ACCEPT_TAIL_CLAMP, na, nt,
+                           None, None, ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, 100 + i, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                           na, nt, None, None, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    peak, src = _peaks()
+    return {"bound": "hbm", "kernel": "rapid_accept (row + select kernels)",
+            "batch": f"{Bb} x {w.n_q} x {w.V} fp32 z and q ({nbytes / 1e6:.1f} MB, > L2)",
+            "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "avg_launch_ms": ms, "peak_source": src + " (hbm_gbs, copy)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -377,12 +426,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
-                    help="named chain workload (default: the 32-layer 120K Llama-3.1-8B step)")
+                    help="named workload (default: the 32-layer 120K Llama-3.1-8B step)")
     args = ap.parse_args()
     from long_context_speculative_gb300 import workloads as wl
     w = wl.LLAMA8B_120K
     if args.workload is not None:
-        w = {x.name: x for x in wl.ALL if not x.tree}[args.workload]
+        w = {x.name: x for x in wl.ALL}[args.workload]
     global WORKLOAD
     WORKLOAD = w.name
     if args.impl == "reference":

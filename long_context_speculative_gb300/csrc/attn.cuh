@@ -23,12 +23,14 @@ struct AttnParams {
     float* LSE;           // [B, Hq, n_q]
     float* part_acc;      // [B*Hkv, nparts, R, d]   un-normalised partial outputs
     float* part_ml;       // [B*Hkv, nparts, R, 2]   (running max m, sum l), log2 domain
+    int* part_nsplit;     // [B*Hkv] splits written per (b, KV head) by the tensor-core kernel
     unsigned int* err;    // sticky device error word
     int64_t cap;          // KV rows per head
     int64_t chunk;        // history rows per split (multiple of 128)
     int B, Hq, Hkv, d, n_q, G, R, S;
     int spec_in_partials; // 1: the history kernel already attended the speculative rows
-    int nparts;           // partial slots per (b, KV head): S, or 2 S for the tensor-core kernel
+    int nparts;           // partial slots per (b, KV head)
+    int balanced;         // 1: splits follow split_of() with pairs = S (tensor-core kernel)
     float scale;          // softmax scale (natural units)
     float scale_log2;     // scale * log2(e)
 };
@@ -39,6 +41,65 @@ __device__ __forceinline__ int64_t clamped_prefix(const AttnParams& p, int b) {
     if (P < 0) P = 0;
     if (P > p.cap - p.n_q) P = p.cap - p.n_q;
     return P;
+}
+
+// Balanced split plan of the tensor-core history kernel, computed the same
+// way by every CTA and by the merge kernel from the device-side prefix
+// lengths: every split gets about the same number of 64-key tiles, so short
+// and long sequences of a ragged batch finish together.  `pairs` is the
+// number of (sequence, split) slots the launch provides per KV head.
+struct SplitOf {
+    int b;        // sequence, or -1 when the slot has no work
+    int s;        // split of that sequence
+    int S_b;      // splits of that sequence
+    int tiles;    // 64-key history tiles of that sequence
+};
+
+__device__ __forceinline__ int seq_tiles(const AttnParams& p, int b) {
+    return (int)((clamped_prefix(p, b) + 63) >> 6);
+}
+
+__device__ __forceinline__ int seq_splits(int tiles, int budget) {
+    const int S = (tiles + budget - 1) / budget;
+    return S < 1 ? 1 : S;
+}
+
+// Smallest tile budget whose splits fit in `pairs` slots (binary search;
+// budget = the longest sequence always fits because pairs >= B).
+__device__ __forceinline__ int split_budget(const AttnParams& p, int pairs) {
+    if (p.B == 1) {
+        const int t = seq_tiles(p, 0);
+        const int budget = (t + pairs - 1) / pairs;
+        return budget < 1 ? 1 : budget;
+    }
+    int total = 0, longest = 1;
+    for (int b = 0; b < p.B; ++b) {
+        const int t = seq_tiles(p, b);
+        total += t;
+        longest = t > longest ? t : longest;
+    }
+    int lo = (total + pairs - 1) / pairs;
+    if (lo < 1) lo = 1;
+    int hi = longest > lo ? longest : lo;
+    while (lo < hi) {
+        const int mid = lo + (hi - lo) / 2;
+        int used = 0;
+        for (int b = 0; b < p.B; ++b) used += seq_splits(seq_tiles(p, b), mid);
+        if (used <= pairs) hi = mid; else lo = mid + 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ SplitOf split_of(const AttnParams& p, int pairs, int c) {
+    const int budget = split_budget(p, pairs);
+    int first = 0;
+    for (int b = 0; b < p.B; ++b) {
+        const int tiles = seq_tiles(p, b);
+        const int S_b = seq_splits(tiles, budget);
+        if (c < first + S_b) return SplitOf{b, c - first, S_b, tiles};
+        first += S_b;
+    }
+    return SplitOf{-1, 0, 0, 0};
 }
 
 // Launchers (return cudaError_t of the launch).

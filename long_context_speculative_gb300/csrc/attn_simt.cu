@@ -202,9 +202,11 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     const int g = bg % p.Hkv;
     const int h = g * p.G + r / p.n_q;
     const int i = r % p.n_q;
-    const int nparts = p.nparts;
-    const float* ml = p.part_ml + ((int64_t)bg * nparts * p.R + r) * 2;     // + s * R * 2
-    const float* pa = p.part_acc + ((int64_t)bg * nparts * p.R + r) * D;    // + s * R * D
+    // partial slots written for this sequence: all S for the CUDA-core
+    // history kernel; S_b of the balanced plan for the tensor-core kernel
+    const int nparts = p.balanced ? p.part_nsplit[bg] : p.nparts;
+    const float* ml = p.part_ml + ((int64_t)bg * p.nparts * p.R + r) * 2;     // + s * R * 2
+    const float* pa = p.part_acc + ((int64_t)bg * p.nparts * p.R + r) * D;    // + s * R * D
     const int64_t mls = (int64_t)p.R * 2, pas = (int64_t)p.R * D;
 
     // ---- speculative rows (warp 0), only when the history kernel skipped them

@@ -191,6 +191,7 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
     int grp_ok[2];        // cleared by a group that failed a wait
+    SplitOf split;        // this CTA's (sequence, split), computed once by thread 0
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block too small");
 
@@ -213,11 +214,17 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int s = blockIdx.x;
-    const int bg = blockIdx.y;
-    const int b = bg / p.Hkv;
-    const int g = bg - b * p.Hkv;
-
+    // blockIdx.x = (sequence, split) slot * row_blocks + row block, blockIdx.y
+    // = KV head.  The row blocks of one split are adjacent CTAs, so they
+    // stream the same K/V tiles together and the second read of each tile is
+    // served from L2.  Which (sequence, split) a slot holds is decided on the
+    // device from the prefix lengths (split_of), after griddep_wait().
+    const int n_rb = (p.R + 127) / 128;
+    const int slot_idx = blockIdx.x / n_rb;
+    const int rb = blockIdx.x - slot_idx * n_rb;
+    const int r0 = rb * 128;                       // first group row of this CTA
+    const int Rb = min(128, p.R - r0);             // rows of this CTA
+    const int g = blockIdx.y;
     // Input-free set-up first: it may overlap the previous kernel in the stream.
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -243,18 +250,30 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     griddep_wait();
+    if (tid == 0) {
+        const SplitOf sp0 = split_of(p, p.S, slot_idx);
+        bars->split = sp0;
+        // the merge kernel reads the number of partials of this (b, g) here
+        if (sp0.b >= 0 && sp0.s == 0 && rb == 0)
+            p.part_nsplit[sp0.b * p.Hkv + g] = sp0.S_b;
+    }
+    __syncthreads();
 
-    // Tiles of this split: the history [0, P) in 64-key tiles, shared out
-    // evenly over the S splits of this (b, g); the last split also takes the
-    // n_q speculative rows [P, P + n_q) as one more, masked, tile.  Tile i is
-    // processed by consumer group i & 1; each group leaves its own partial.
+    // Tiles of this split: the history [0, P) of sequence b in 64-key tiles,
+    // shared out evenly over its S_b splits; the last split also takes the n_q
+    // speculative rows [P, P + n_q) as one more, masked, tile.
+    const SplitOf sp = bars->split;
+    const bool has_work = sp.b >= 0;
+    const int b = has_work ? sp.b : 0;
+    const int s = sp.s;
+    const int bg = b * p.Hkv + g;
     const int64_t P = clamped_prefix(p, b);
-    const int n_all = (int)((P + kKeys - 1) / kKeys);
-    const int t_begin = (int)(((int64_t)s * n_all) / p.S);
-    const int t_end = (int)(((int64_t)(s + 1) * n_all) / p.S);
+    const int n_all = sp.tiles;
+    const int t_begin = has_work ? (int)(((int64_t)s * n_all) / sp.S_b) : 0;
+    const int t_end = has_work ? (int)(((int64_t)(s + 1) * n_all) / sp.S_b) : 0;
     const int n_hist = t_end - t_begin;
-    const bool spec_here = (s == p.S - 1);
-    const int n = n_hist + (spec_here ? 1 : 0);
+    const bool spec_here = has_work && (s == sp.S_b - 1);
+    const int n = has_work ? n_hist + (spec_here ? 1 : 0) : 0;
     const int64_t slot = ((int64_t)bg * p.nparts + s) * p.R;
 
     // Q rows of the group into shared memory (K-major, 128-byte swizzle);
@@ -262,10 +281,10 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     if (tid < ROWS && n > 0) {
         const int r = tid;
         uint4 chunk[16];
-        if (r < p.R) {
+        if (r < Rb) {
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const __nv_bfloat16*>(p.Q) +
-                (((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q + r) * kD);
+                (((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q + r0 + r) * kD);
 #pragma unroll
             for (int j = 0; j < 16; ++j) chunk[j] = src[j];
         } else {
@@ -280,9 +299,9 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
         fence_proxy_async_smem();
     }
-    if (n <= 0 && tid < p.R) {   // empty split: m = -inf, l = 0 (no tile touched)
-        p.part_ml[(slot + tid) * 2 + 0] = -INFINITY;
-        p.part_ml[(slot + tid) * 2 + 1] = 0.f;
+    if (has_work && n <= 0 && tid < Rb) {   // empty split: m = -inf, l = 0
+        p.part_ml[(slot + r0 + tid) * 2 + 0] = -INFINITY;
+        p.part_ml[(slot + r0 + tid) * 2 + 1] = 0.f;
     }
     tc_fence_before();
     __syncthreads();
@@ -420,8 +439,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         const int64_t key_end = ((int64_t)t_end * kKeys < P) ? (int64_t)t_end * kKeys : P;
         // visibility of the n_q speculative keys for this row (the masked tile)
         uint64_t spec_bits = 0;
-        if (spec_here && ((n - 1) & 1) == gr && r < p.R) {
-            const int iq = r % p.n_q;
+        if (spec_here && ((n - 1) & 1) == gr && r < Rb) {
+            const int iq = (r0 + r) % p.n_q;
             for (int j = 0; j < p.n_q; ++j) {
                 const bool vis =
                     p.mask ? (p.mask[((int64_t)b * p.n_q + iq) * p.n_q + j] != 0) : (j <= iq);
@@ -543,9 +562,9 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             const float w1 = has1 ? ex2(m1 - M) : 0.f;
             // tcgen05.ld is warp-collective (.sync.aligned): every lane
             // executes the same loads; only the stores are per-row.
-            const bool real_row = r < p.R;
+            const bool real_row = r < Rb;
             const int half = gr;                      // this warp's 64 output columns
-            float* dst = p.part_acc + (slot + r) * kD + half * 64;
+            float* dst = p.part_acc + (slot + r0 + r) * kD + half * 64;
 #pragma unroll
             for (int qq = 0; qq < 2; ++qq) {
                 uint32_t o0[32], o1[32];
@@ -565,8 +584,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 }
             }
             if (real_row && half == 0) {
-                p.part_ml[(slot + r) * 2 + 0] = M;
-                p.part_ml[(slot + r) * 2 + 1] = l0 * w0 + l1 * w1;
+                p.part_ml[(slot + r0 + r) * 2 + 0] = M;
+                p.part_ml[(slot + r0 + r) * 2 + 1] = l0 * w0 + l1 * w1;
             }
         }
         if (!ok) bars->abort = 1;
@@ -612,7 +631,7 @@ bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
 
 bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
     if (dtype != 1 || p.d != kD) return false;
-    if (p.R < 1 || p.R > 128) return false;
+    if (p.R < 1 || p.R > 512) return false;      // up to four 128-row blocks
     if ((int64_t)p.B * p.Hkv * p.cap >= ((int64_t)1 << 31)) return false;
     return tensor_map_encoder() != nullptr;
 }
@@ -627,7 +646,7 @@ cudaError_t launch_rows(const CUtensorMap& tmK, const CUtensorMap& tmV, const At
                                          Plan<ROWS>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.S, p.B * p.Hkv, 1);
+    cfg.gridDim = dim3(p.S * ((p.R + 127) / 128), p.Hkv, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Plan<ROWS>::kSmemBytes;
     cfg.stream = st;

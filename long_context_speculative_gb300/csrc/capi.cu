@@ -69,11 +69,19 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     const int sms = sm_count();
     int64_t chunk;
     if (pl.tc) {
-        // One CTA per SM, one wave: spread B * Hkv heads over the SMs.
-        const int64_t heads = (int64_t)B * Hkv;
-        int64_t S = sms / heads;
-        if (S < 1) S = 1;
-        chunk = (max_prefix + S - 1) / S;
+        // One CTA per SM, one wave: (sequence, split) slots per KV head, times
+        // the 128-row blocks of a wide group.  The kernel decides on the
+        // device how the slots are shared out over the sequences.
+        const int64_t per_slot = (int64_t)Hkv * ((R + 127) / 128);
+        int64_t S = sms / per_slot;
+        if (S < B) S = B;
+        pl.S = (int)S;
+        pl.nparts = (int)S;
+        pl.chunk = 0;
+        const size_t part = (size_t)B * Hkv * pl.nparts * R;
+        pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float)) +
+                      align_up((size_t)B * Hkv * sizeof(int));
+        return pl;
     } else {
         const int64_t rbs = (R + 63) / 64;
         const int64_t ctas = (int64_t)B * Hkv * rbs;
@@ -94,7 +102,8 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     pl.chunk = chunk;
     pl.nparts = (int)S;
     const size_t part = (size_t)B * Hkv * pl.nparts * R;
-    pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float));
+    pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float)) +
+                  align_up((size_t)B * Hkv * sizeof(int));
     return pl;
 }
 
@@ -132,6 +141,7 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.n_q = n_q; p.G = Hq / Hkv; p.R = p.G * n_q;
     p.S = pl.S;
     p.spec_in_partials = pl.tc ? 1 : 0;
+    p.balanced = pl.tc ? 1 : 0;
     p.nparts = pl.nparts;
     p.err = device_error_word();
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)d);
@@ -140,6 +150,9 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
     p.part_acc = static_cast<float*>(workspace);
     p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                          align_up(part * d * sizeof(float)));
+    p.part_nsplit = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                           align_up(part * d * sizeof(float)) +
+                                           align_up(part * 2 * sizeof(float)));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = pl.tc ? launch_attn_prefix_tc(p, st) : launch_attn_prefix_simt(p, dtype, st);
     if (e != cudaSuccess) return RAPID_ECUDA;

@@ -75,7 +75,13 @@ QWEN7B_TREE = Workload("qwen2.5-7b_tree32_28layers", B=4, Hq=28, Hkv=4, d=128, n
                        z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
                        tree=True, seed=1005)
 
-ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA8B_1LAYER_120K, LLAMA70B_128K, QWEN7B_TREE]
+QWEN7B_TREE_1LAYER = Workload("qwen2.5-7b_tree32_1layer", B=4, Hq=28, Hkv=4, d=128, n_q=32,
+                              prefix=98304, prefix_lo=32768, layers=1, V=152064, dtype="bf16",
+                              z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
+                              tree=True, seed=1005)
+
+ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA8B_1LAYER_120K, LLAMA70B_128K, QWEN7B_TREE,
+       QWEN7B_TREE_1LAYER]
 
 
 def gen(seed: int, device="cpu") -> torch.Generator:
