@@ -8,16 +8,31 @@
 // entries of p_hat below 0.1 * max p_hat replaced by those of p, p_hat used in
 // the ratio test, and the adjusted residual norm(max(p - p_hat, p - q)).
 //
-// Layout of the work: one thread-block cluster per vocabulary row (b, j); the
-// row is cut into `chunk`-sized pieces, one per CTA, bulk-copied (TMA) into
-// shared memory.  Three vocabulary-wide reductions (the softmax of z/T, the
-// softmax of the augmented logits, the residual mass) combine across the
-// cluster through distributed shared memory.  Every row settles the ratio test
-// of each draft node scored by it and draws its one candidate next token
-// (uniform u_{j+1}): the adjusted residual if the row has children, else the
-// bonus draw from p.  A second small kernel walks the chain or tree and picks
-// n_accepted and the next token from those per-row results.
+// Layout of the work.  A row of V entries is cut into C slices, one per CTA
+// of a thread-block cluster; the clusters are persistent and cluster c takes
+// rows c, c + nclusters, ...  Each CTA keeps its slice of the next rows'
+// (z, q) in shared memory through a ring of bulk (TMA) copies, so the next
+// rows stream in while the current one is worked on.  A row needs two
+// vocabulary-wide reductions -- the softmax of z/T and the softmax of the
+// augmented logits -- which every CTA completes from the C slice partials
+// that its peers send it with st.async into its shared memory (completion on
+// an mbarrier, double-buffered by row parity).  Two rows are in flight per
+// CTA: while the partials of row i travel, the CTA finishes row i - 1: the
+// ratio tests of the draft nodes scored by that row, and the row's residual
+// mass per slice (its p mass per slice follows from the first reduction).
+// The selection kernel then walks the chain or tree, picks n_accepted, and
+// draws the next token from the one row it needs: it finds the slice that
+// holds the inverse-CDF target from the per-slice masses and scans only that
+// slice.
+//
+// Exponentials are taken against one reference per warp: the warp's max of x
+// for p, and for the augmented logits a = x + eta (q - p) the bound
+// max x + eta (a <= x + eta since q <= 1 and p >= 0; for eta > 32, where
+// exp(a - bound) could underflow, the warp's exact max of a).  Sums carry
+// their reference and are rescaled when combined.
 #include <cooperative_groups.h>
+
+#include <mutex>
 
 #include "accept.cuh"
 #include "common.cuh"
@@ -28,47 +43,96 @@ namespace rapid {
 
 namespace {
 
-constexpr int kNT = kAcceptThreads;
-constexpr int kWarps = kNT / 32;
+constexpr int kRT = kAcceptRowThreads;
+constexpr int kST = kAcceptSelThreads;
+constexpr int kSW = kST / 32;
+constexpr size_t kSmemBudget = (size_t)2 * kAcceptMaxSlice * 8;   // dynamic shared memory for the row ring
+constexpr int kMinSlice = 1024;          // rows shorter than C x this use fewer slices
+constexpr float kEtaBound = 32.f;        // largest eta for which max x + eta is the reference of a
 
-struct MS {
-    float m, s;
-};
-
-// (m_a, s_a) + (m_b, s_b) for sums of exp(x - m): rescale to the larger max.
-__device__ __forceinline__ MS ms_combine(MS a, MS b) {
-    const float m = fmaxf(a.m, b.m);
-    if (m == -INFINITY) return MS{-INFINITY, 0.f};
-    const float sa = a.s > 0.f ? a.s * exp2f((a.m - m) * kLog2e) : 0.f;
-    const float sb = b.s > 0.f ? b.s * exp2f((b.m - m) * kLog2e) : 0.f;
-    return MS{m, sa + sb};
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__device__ __forceinline__ MS warp_ms(MS v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        MS w;
-        w.m = __shfl_xor_sync(0xffffffffu, v.m, o);
-        w.s = __shfl_xor_sync(0xffffffffu, v.s, o);
-        v = ms_combine(v, w);
-    }
+// Two-lane packed fp32 arithmetic (one instruction for both lanes).
+__device__ __forceinline__ uint64_t pack2(float2 v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
     return v;
 }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(d);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
+    return unpack2(d);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// Max over the 32 lanes (all lanes active), the same in every lane.
+__device__ __forceinline__ float redux_max(float v) {
+    float d;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(d) : "f"(v));
+    return d;
+}
 
-struct RowShared {
-    uint64_t bar;
-    int n_children;
-    int children[kAcceptMaxNq];
-    MS red_ms[kWarps];
-    float red_f[kWarps][16];
-    float stripe_total[16];
-    float warp_tot[kWarps];
-    // cluster exchange slots (read by peers through distributed shared memory)
-    MS x_ms1;
-    MS x_ms2;
-    float x_w;
-    int pick_thread;
-    int last_thread;
+struct MS {
+    float m, s;   // a sum of exp(x - m)
+};
+
+// Combine the (m, s) of the 32 lanes; the result is the same in every lane.
+__device__ __forceinline__ MS warp_ms(MS v) {
+    const float m = redux_max(v.m);
+    const float s = v.s > 0.f ? v.s * ex2((v.m - m) * kLog2e) : 0.f;
+    return MS{m, warp_sum(s)};
+}
+
+constexpr int kGroups = 2;               // warp groups of a row-kernel CTA, one row each
+constexpr int kGT = kRT / kGroups;       // threads of a group
+constexpr int kGW = kGT / 32;            // warps of a group
+
+struct RowsShared {
+    uint64_t full[kGroups];   // the group's (z, q) slice landed
+    uint64_t mb1[kGroups];    // slice partials of reduction 1 received
+    uint64_t mb2[kGroups];    // slice partials of reduction 2 received
+    float2 recv1[kGroups][kAcceptMaxCluster];   // (m, s) of x per slice
+    float2 recv2[kGroups][kAcceptMaxCluster];   // (reference, s) of a per slice
+    float recv2a[kGroups][kAcceptMaxCluster];   // max of a per slice
+    float2 red1[kGroups][kGW];   // per-warp partials of the group's row
+    float2 red2[kGroups][kGW];
+    float red2a[kGroups][kGW];
+    float red3[kGroups][kGW];
+    float2 part1[kGroups];       // this slice's (m, s) of x
+    int arrived[kGroups][3];     // warps of the group done with pass 1, pass 2, the finish
+    int abort;                   // a wait gave up: stop waiting, let the kernel run out
 };
 
 __device__ __forceinline__ int parent_of(const AcceptParams& p, int b, int i) {
@@ -79,394 +143,734 @@ __device__ __forceinline__ int parent_of(const AcceptParams& p, int b, int i) {
     return par;
 }
 
-// Block-wide (m, s) combine; result valid in every thread.
-__device__ MS block_ms(MS v, RowShared& sh) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    v = warp_ms(v);
-    __syncthreads();
-    if (lane == 0) sh.red_ms[warp] = v;
-    __syncthreads();
-    MS acc = sh.red_ms[0];
-    for (int w = 1; w < kWarps; ++w) acc = ms_combine(acc, sh.red_ms[w]);
-    return acc;
+__device__ __forceinline__ void group_sync(int g) {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(kGT) : "memory");
+}
+
+// A warp of the group is done with a phase (its slot written by lane 0):
+// true, in every lane, for the last warp of the group to get there, which
+// then sees every warp's slot.  The counter is reset by that warp.
+__device__ __forceinline__ bool group_arrive(int* counter) {
+    const int lane = threadIdx.x & 31;
+    int last = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        last = atomicAdd(counter, 1) == kGW - 1;
+        if (last) {
+            *counter = 0;
+            __threadfence_block();
+        }
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    __syncwarp();
+    return last != 0;
+}
+
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, float a, float b, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+        "f"(a), "f"(b), "r"(rbar)
+        : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float a, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(raddr),
+                 "f"(a), "r"(rbar)
+                 : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  After a wait gave up (one second), the
+// CTA stops waiting altogether; the error word records where.
+__device__ __forceinline__ void wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned int* err, unsigned int code) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_timer_ns();
+    while (!*abort) {
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            if (err) {
+                atomicOr(err, kErrWaitTimeout);
+                atomicCAS(err + 1, 0u, code | 0x80000000u);
+            }
+            return;
+        }
+    }
+}
+
+// Per-thread state of the row a group works on.
+template <int F>
+struct RowState {
+    float e[4 * F];   // exp(x - mw) of this thread's entries (x = z / T)
+    float mw;         // warp max of x
+    float fw;         // exp(mw - m1) / s1: p = e * fw
+    float rw;         // warp reference of the augmented logits
+    float m1, s1;     // row softmax statistics of x (after reduction 1)
+};
+
+// Group thread t owns float4 groups t, t + kGT, ... of a row array of G groups (G
+// a multiple of 32, so validity is warp-uniform).  Entries past the slice
+// hold z = -inf and q = 0, which give p = 0, h = 0 and a residual weight of
+// 0, so the passes need no per-entry bounds checks.
+template <int F>
+__device__ __forceinline__ bool group_valid(int f, int G) {
+    return f < F - 1 || (int)(threadIdx.x % kGT) + f * kGT < G;
+}
+
+// Pass 1: x = z / T; exp(x - mw) with mw the warp max; the warp's (mw, sum).
+template <int F>
+__device__ __forceinline__ MS pass1(RowState<F>& st, const float* zb, int G, float invT) {
+    const int t = threadIdx.x % kGT;
+    const float2 it2 = make_float2(invT, invT);
+    float mt = -INFINITY;
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+        if (group_valid<F>(f, G)) {
+            const float4 r = *reinterpret_cast<const float4*>(zb + 4 * (t + f * kGT));
+            const float2 x01 = mul2(make_float2(r.x, r.y), it2);
+            const float2 x23 = mul2(make_float2(r.z, r.w), it2);
+            st.e[4 * f] = x01.x; st.e[4 * f + 1] = x01.y;
+            st.e[4 * f + 2] = x23.x; st.e[4 * f + 3] = x23.y;
+            mt = max3(mt, x01.x, x01.y);
+            mt = max3(mt, x23.x, x23.y);
+        }
+    }
+    const float mw = redux_max(mt);
+    const float mb = mw == -INFINITY ? 0.f : mw * kLog2e;
+    const float2 l2 = make_float2(kLog2e, kLog2e), nb = make_float2(-mb, -mb);
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+        if (group_valid<F>(f, G)) {
+            const float2 g01 = fma2(make_float2(st.e[4 * f], st.e[4 * f + 1]), l2, nb);
+            const float2 g23 = fma2(make_float2(st.e[4 * f + 2], st.e[4 * f + 3]), l2, nb);
+            const float2 e01 = make_float2(ex2(g01.x), ex2(g01.y));
+            const float2 e23 = make_float2(ex2(g23.x), ex2(g23.y));
+            st.e[4 * f] = e01.x; st.e[4 * f + 1] = e01.y;
+            st.e[4 * f + 2] = e23.x; st.e[4 * f + 3] = e23.y;
+            s = add2(s, e01);
+            s = add2(s, e23);
+        }
+    }
+    st.mw = mw;
+    return MS{mw, warp_sum(s.x + s.y)};
+}
+
+// Pass 2: p = e * fw; a = x + eta (q - p); h = exp(a - rw) stored over z in
+// shared memory (-inf past the slice end n, which keeps the padding intact);
+// the warp's (rw, sum) and its max of a.
+template <int F>
+__device__ __forceinline__ MS pass2(RowState<F>& st, float* zb, const float* qb, int G, int n,
+                                    float invT, float eta, float* amax_w) {
+    const int t = threadIdx.x % kGT;
+    const float fw = st.mw == -INFINITY ? 0.f : ex2((st.mw - st.m1) * kLog2e) / st.s1;
+    st.fw = fw;
+    const float2 it2 = make_float2(invT, invT), nf2 = make_float2(-fw, -fw);
+    const float2 eta2 = make_float2(eta, eta);
+    float rw;
+    if (eta <= kEtaBound) {
+        rw = st.mw == -INFINITY ? -INFINITY : st.mw + eta;
+    } else {
+        float am = -INFINITY;
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+            if (group_valid<F>(f, G)) {
+                const int el = 4 * (t + f * kGT);
+                const float4 z4 = *reinterpret_cast<const float4*>(zb + el);
+                const float4 q4 = *reinterpret_cast<const float4*>(qb + el);
+                const float2 a01 = fma2(eta2, fma2(make_float2(st.e[4 * f], st.e[4 * f + 1]), nf2,
+                                                   make_float2(q4.x, q4.y)),
+                                        mul2(make_float2(z4.x, z4.y), it2));
+                const float2 a23 = fma2(eta2, fma2(make_float2(st.e[4 * f + 2], st.e[4 * f + 3]), nf2,
+                                                   make_float2(q4.z, q4.w)),
+                                        mul2(make_float2(z4.z, z4.w), it2));
+                am = max3(am, a01.x, a01.y);
+                am = max3(am, a23.x, a23.y);
+            }
+        }
+        rw = redux_max(am);
+    }
+    const float rb = rw == -INFINITY ? 0.f : rw * kLog2e;
+    const float2 l2 = make_float2(kLog2e, kLog2e), nb = make_float2(-rb, -rb);
+    float amax = -INFINITY;
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+        if (group_valid<F>(f, G)) {
+            const int el = 4 * (t + f * kGT);
+            const float4 z4 = *reinterpret_cast<const float4*>(zb + el);
+            const float4 q4 = *reinterpret_cast<const float4*>(qb + el);
+            const float2 a01 = fma2(eta2, fma2(make_float2(st.e[4 * f], st.e[4 * f + 1]), nf2,
+                                               make_float2(q4.x, q4.y)),
+                                    mul2(make_float2(z4.x, z4.y), it2));
+            const float2 a23 = fma2(eta2, fma2(make_float2(st.e[4 * f + 2], st.e[4 * f + 3]), nf2,
+                                               make_float2(q4.z, q4.w)),
+                                    mul2(make_float2(z4.z, z4.w), it2));
+            amax = max3(amax, a01.x, a01.y);
+            amax = max3(amax, a23.x, a23.y);
+            const float2 g01 = fma2(a01, l2, nb);
+            const float2 g23 = fma2(a23, l2, nb);
+            float4 h = make_float4(ex2(g01.x), ex2(g01.y), ex2(g23.x), ex2(g23.y));
+            // same pairing and order of additions as pass 1, so that eta = 0
+            // gives p_hat == p bit for bit
+            s = add2(s, make_float2(h.x, h.y));
+            s = add2(s, make_float2(h.z, h.w));
+            if (el + 4 > n) {
+                if (el >= n) h.x = -INFINITY;
+                if (el + 1 >= n) h.y = -INFINITY;
+                if (el + 2 >= n) h.z = -INFINITY;
+                h.w = -INFINITY;
+            }
+            *reinterpret_cast<float4*>(zb + el) = h;
+        }
+    }
+    st.rw = rw;
+    *amax_w = redux_max(amax);
+    return MS{rw, warp_sum(s.x + s.y)};
 }
 
 template <int F>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kRT, 1)
 accept_rows_kernel(const AcceptParams p) {
-    constexpr int E = 4 * F;
     cg::cluster_group cluster = cg::this_cluster();
-    const int C = (int)cluster.num_blocks();
+    const int C = p.C;
+    const int G = p.groups;
+    const int span = 4 * G;
     const int rank = (int)cluster.block_rank();
-    const int row = blockIdx.y;                 // b * n_q + j
-    const int b = row / p.n_q;
-    const int j = row - b * p.n_q;
+    const int cid = (int)(blockIdx.x / C);
     const int t = threadIdx.x;
+    const int g = t / kGT;           // warp group: local rows g, g + 2, g + 4, ...
+    const int tg = t % kGT;
+    const int wg = tg >> 5, lane = t & 31;
 
     extern __shared__ float4 dyn_f4[];
-    float* sz = reinterpret_cast<float*>(dyn_f4);
-    float* sq = sz + p.chunk;
-    __shared__ RowShared sh;
-    griddep_wait();
+    float* bufs = reinterpret_cast<float*>(dyn_f4);
+    __shared__ RowsShared sh;
 
     const int64_t lo = (int64_t)rank * p.chunk;
     int64_t n64 = (int64_t)p.V - lo;
     if (n64 > p.chunk) n64 = p.chunk;
     if (n64 < 0) n64 = 0;
     const int n = (int)n64;
-    const float* zrow = p.z + (int64_t)row * p.V + lo;
-    const float* qrow = p.q + (int64_t)row * p.V + lo;
+    const int nrows = cid < p.rows ? (p.rows - cid + p.nclusters - 1) / p.nclusters : 0;
 
-    // ---- stage this CTA's piece of z and q in shared memory -------------
+    if (t == 0) {
+        for (int i = 0; i < kGroups; ++i) {
+            mbar_init(&sh.full[i], 1);
+            mbar_init(&sh.mb1[i], 1);
+            mbar_init(&sh.mb2[i], 1);
+            sh.arrived[i][0] = sh.arrived[i][1] = sh.arrived[i][2] = 0;
+        }
+        sh.abort = 0;
+        fence_mbar_init();
+    }
+    // padding past the slice: z = -inf, q = 0 (bulk copies never write there)
+    for (int b = 0; b < kGroups; ++b) {
+        float* zb = bufs + (size_t)b * 2 * span;
+        for (int e = n + t; e < span; e += kRT) {
+            zb[e] = -INFINITY;
+            zb[span + e] = 0.f;
+        }
+    }
+    cluster.sync();   // barriers and padding in place before any copy or peer send
+    griddep_wait();
+
+    float* zb = bufs + (size_t)g * 2 * span;   // this group's row buffer
+    float* qb = zb + span;
+    auto row_of = [&](int i) -> int64_t { return cid + (int64_t)i * p.nclusters; };
+    auto load_row = [&](int i) {      // one thread, bulk path
+        mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 8));
+        if (n > 0) {
+            const int64_t off = row_of(i) * p.V + lo;
+            bulk_g2s(zb, p.z + off, (uint32_t)(n * 4), &sh.full[g]);
+            bulk_g2s(qb, p.q + off, (uint32_t)(n * 4), &sh.full[g]);
+        }
+    };
+    // L2 prefetch of a later row of this group, so that its bulk copy, issued
+    // only once the buffer is free, is served from L2
+    auto prefetch_row = [&](int i) {   // one thread, bulk path
+        if (i < nrows && n > 0) {
+            const int64_t off = row_of(i) * p.V + lo;
+            bulk_prefetch_l2(p.z + off, (uint32_t)(n * 4));
+            bulk_prefetch_l2(p.q + off, (uint32_t)(n * 4));
+        }
+    };
+    if (p.bulk && tg == 0 && g < nrows) load_row(g);
+
+    // The group's last two warps run the ratio tests: thread tg handles child
+    // c = tg - (kGT - kAcceptMaxNq).  Its token and parent are loaded a row ahead.
+    const int c = tg - (kGT - kAcceptMaxNq);
+    const bool rt_thread = c >= 0 && c < p.n_q;
+    int pf_tok = -1, pf_par = -1;
+    auto prefetch_node = [&](int i) {
+        if (rt_thread && i < nrows) {
+            const int b = (int)(row_of(i) / p.n_q);
+            pf_tok = p.tokens[(int64_t)b * p.n_q + c];
+            pf_par = c == 0 ? -1 : parent_of(p, b, c);
+        }
+    };
+    prefetch_node(g);
+
+    RowState<F> st;
+    // Each row: its copy lands, pass 1, reduction 1 across the cluster, pass 2,
+    // reduction 2, then the ratio tests and the residual mass.  Warps move on
+    // independently; the last warp of a phase combines the group's partials
+    // and sends them to the cluster, and every warp waits for the cluster's
+    // partials itself.  The other group computes while this one waits.
+#pragma unroll 1
+    for (int k = 0;; ++k) {
+        const int i = 2 * k + g;
+        if (i >= nrows) break;
+        const int64_t row = row_of(i);
+        const int b = (int)(row / p.n_q);
+        const int j = (int)(row - (int64_t)b * p.n_q);
+        if (tg == 0) {
+            // arm this row's exchange barriers (their previous phases completed
+            // before any warp of the group could finish the previous row)
+            mbar_arrive_expect_tx(&sh.mb1[g], (uint32_t)(C * 8));
+            mbar_arrive_expect_tx(&sh.mb2[g], (uint32_t)(C * 12));
+            if (p.bulk) prefetch_row(i + 2);
+        }
+        const int my_tok = pf_tok, my_par = pf_par;
+        prefetch_node(i + 2);
+        if (p.bulk) {
+            wait_or_abort(&sh.full[g], (uint32_t)(k & 1), &sh.abort, p.err,
+                          0x01000000u | (unsigned)(i & 0xffff));
+        } else {
+            const int64_t off = row * p.V + lo;
+            for (int e = tg; e < n; e += kGT) {
+                zb[e] = p.z[off + e];
+                qb[e] = p.q[off + e];
+            }
+            group_sync(g);
+        }
+        // z and q at the token of child c of this row, for its ratio test
+        int key = -1;
+        float2 zq = make_float2(0.f, 0.f);
+        if (rt_thread && c > j && my_par == j) {
+            if (my_tok < 0 || my_tok >= p.V) {
+                key = rank == 0 ? -2 : -1;
+            } else if (my_tok >= lo && my_tok < lo + n) {
+                key = my_tok;
+                zq = make_float2(zb[my_tok - lo], qb[my_tok - lo]);
+            }
+        }
+        // pass 1; the group's last warp sends the slice's (m, s) to the cluster
+        {
+            const MS w1 = pass1<F>(st, zb, G, p.invT);
+            if (lane == 0) sh.red1[g][wg] = make_float2(w1.m, w1.s);
+            if (group_arrive(&sh.arrived[g][0])) {
+                const float2 x = lane < kGW ? sh.red1[g][lane] : make_float2(-INFINITY, 0.f);
+                const MS c1 = warp_ms(MS{x.x, x.y});
+                if (lane == 0) {   // read back after reduction 1 completes, which this send is part of
+                    sh.part1[g] = make_float2(c1.m, c1.s);
+                    __threadfence_block();
+                }
+                __syncwarp();
+                if (lane < C)
+                    st_async_v2(mapa_u32(smem_u32(&sh.recv1[g][rank]), (uint32_t)lane), c1.m, c1.s,
+                                mapa_u32(smem_u32(&sh.mb1[g]), (uint32_t)lane));
+            }
+        }
+        // uniform r_c of the ratio test, while the cluster reduces
+        float r_c = 0.f;
+        if (key >= 0) {
+            const Philox4 rnd = philox4x32_10((uint32_t)c, (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
+            r_c = word_uniform(rnd.w[0]);
+        }
+        wait_or_abort(&sh.mb1[g], (uint32_t)(k & 1), &sh.abort, p.err,
+                      0x03000000u | (unsigned)(i & 0xffff));
+        {
+            MS r1{-INFINITY, 0.f};
+            if (lane < C) r1 = MS{sh.recv1[g][lane].x, sh.recv1[g][lane].y};
+            r1 = warp_ms(r1);
+            st.m1 = r1.m;
+            st.s1 = r1.s;
+        }
+        // pass 2; the group's last warp sends the slice's (reference, s, max a)
+        {
+            float amw;
+            const MS w2 = pass2<F>(st, zb, qb, G, n, p.invT, p.eta, &amw);
+            if (lane == 0) {
+                sh.red2[g][wg] = make_float2(w2.m, w2.s);
+                sh.red2a[g][wg] = amw;
+            }
+            if (group_arrive(&sh.arrived[g][1])) {
+                const float2 x = lane < kGW ? sh.red2[g][lane] : make_float2(-INFINITY, 0.f);
+                const MS c2 = warp_ms(MS{x.x, x.y});
+                const float ac = redux_max(lane < kGW ? sh.red2a[g][lane] : -INFINITY);
+                if (lane < C) {
+                    const uint32_t rbar = mapa_u32(smem_u32(&sh.mb2[g]), (uint32_t)lane);
+                    st_async_v2(mapa_u32(smem_u32(&sh.recv2[g][rank]), (uint32_t)lane), c2.m, c2.s, rbar);
+                    st_async_f32(mapa_u32(smem_u32(&sh.recv2a[g][rank]), (uint32_t)lane), ac, rbar);
+                }
+                if (lane == 0) {   // p mass of this slice
+                    const float2 c1 = sh.part1[g];
+                    p.ws_mass[(row * kAcceptMaxCluster + rank) * 2 + 1] =
+                        c1.y > 0.f ? c1.y * ex2((c1.x - st.m1) * kLog2e) / st.s1 : 0.f;
+                }
+            }
+        }
+        wait_or_abort(&sh.mb2[g], (uint32_t)(k & 1), &sh.abort, p.err,
+                      0x02000000u | (unsigned)(i & 0xffff));
+        float m2, s2;
+        {
+            MS r2{-INFINITY, 0.f};
+            float am = -INFINITY;
+            if (lane < C) {
+                r2 = MS{sh.recv2[g][lane].x, sh.recv2[g][lane].y};
+                am = sh.recv2a[g][lane];
+            }
+            r2 = warp_ms(r2);
+            am = redux_max(am);
+            // (m2, s2) with m2 the row max of a, so that max p_hat = 1 / s2
+            m2 = am;
+            s2 = r2.m == am ? r2.s : r2.s * ex2((r2.m - am) * kLog2e);
+        }
+        const float thr = p.clamp ? 0.1f / s2 : -1.0f;
+        // ratio test of child c
+        const int64_t node = (int64_t)b * p.n_q + c;
+        if (key >= 0) {
+            const float x = zq.x * p.invT;
+            const float pt = ex2((x - st.m1) * kLog2e) / st.s1;
+            const float a = fmaf(p.eta, zq.y - pt, x);
+            float ph = ex2((a - m2) * kLog2e) / s2;
+            if (ph < thr) ph = pt;
+            const float ratio = zq.y == 0.f ? INFINITY : ph / zq.y;
+            p.ws_accept[node] = r_c <= fminf(1.0f, ratio) ? 1 : 0;
+            if (p.diag) {
+                float* dg = p.diag + node * 5;
+                dg[0] = pt; dg[1] = ph; dg[2] = zq.y; dg[3] = ratio; dg[4] = r_c;
+            }
+        } else if (key == -2) {
+            p.ws_accept[node] = 0;   // token outside the vocabulary: reject
+        }
+        // residual mass of the slice
+        const float gw = st.rw == -INFINITY ? 0.f : ex2((st.rw - m2) * kLog2e) / s2;
+        const float2 fw2 = make_float2(st.fw, st.fw), gw2 = make_float2(gw, gw);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+            if (group_valid<F>(f, G)) {
+                const int el = 4 * (tg + f * kGT);
+                const float4 h4 = *reinterpret_cast<const float4*>(zb + el);
+                const float4 q4 = *reinterpret_cast<const float4*>(qb + el);
+                const float2 p01 = mul2(make_float2(st.e[4 * f], st.e[4 * f + 1]), fw2);
+                const float2 p23 = mul2(make_float2(st.e[4 * f + 2], st.e[4 * f + 3]), fw2);
+                float2 h01 = mul2(make_float2(h4.x, h4.y), gw2);
+                float2 h23 = mul2(make_float2(h4.z, h4.w), gw2);
+                if (h01.x < thr) h01.x = p01.x;
+                if (h01.y < thr) h01.y = p01.y;
+                if (h23.x < thr) h23.x = p23.x;
+                if (h23.y < thr) h23.y = p23.y;
+                // max(p - p_hat, p - q, 0) = p - min(p, p_hat, q); padding
+                // (h = -inf, q = 0, p = 0) gives 0, min3 drops the NaN of -inf * 0
+                const float2 m01 = make_float2(min3(p01.x, h01.x, q4.x), min3(p01.y, h01.y, q4.y));
+                const float2 m23 = make_float2(min3(p23.x, h23.x, q4.z), min3(p23.y, h23.y, q4.w));
+                acc = add2(acc, sub2(p01, m01));
+                acc = add2(acc, sub2(p23, m23));
+            }
+        }
+        const float wsum = warp_sum(acc.x + acc.y);
+        if (lane == 0) sh.red3[g][wg] = wsum;
+        if (group_arrive(&sh.arrived[g][2])) {
+            // every warp of the group is done with the buffer
+            const float tot = warp_sum(lane < kGW ? sh.red3[g][lane] : 0.f);
+            if (lane == 0) {
+                p.ws_mass[(row * kAcceptMaxCluster + rank) * 2] = tot;
+                if (rank == 0) {
+                    float* sts = p.ws_stats + row * 4;
+                    sts[0] = st.m1; sts[1] = st.s1; sts[2] = m2; sts[3] = s2;
+                }
+                // the group's buffer takes its next row
+                if (p.bulk && i + 2 < nrows) {
+                    fence_proxy_async_smem();
+                    load_row(i + 2);
+                }
+            }
+        }
+        if (!p.bulk) group_sync(g);   // the synchronous copy of the next row overwrites the buffer
+    }
+    __syncthreads();   // both groups done: no copy of this CTA is outstanding unless a wait gave up
+    if (t == 0) {
+        griddep_launch_dependents();
+        if (p.bulk && sh.abort) {
+            // a wait gave up: let the groups' last copies land before the CTA exits
+            for (int gg = 0; gg < kGroups; ++gg) {
+                const int nmine = nrows > gg ? (nrows - gg + 1) / 2 : 0;
+                if (nmine > 0) mbar_wait(&sh.full[gg], (uint32_t)((nmine - 1) & 1), nullptr);
+            }
+        }
+    }
+    // no CTA leaves while a peer may still deliver into its shared memory
+    cluster.sync();
+}
+
+// One CTA per sequence: pick the winning path, then draw the next token from
+// row e (the last accepted node) by inverse CDF in token-id order with u_{e+1}:
+// the residual if e has children, else p (the bonus draw).
+__global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p) {
+    extern __shared__ float4 sel_dyn[];
+    float* sz = reinterpret_cast<float*>(sel_dyn);   // [chunk] z of the slice, then its weights
+    float* sq = sz + p.chunk;                        // [chunk] q of the slice
+    __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq];
+    __shared__ int s_key[2];
+    __shared__ int s_e, s_has_children, s_resid, s_owner, s_ow;
+    __shared__ float s_tin, s_tw;
+    __shared__ float s_seg[kSW];
+    __shared__ __align__(8) uint64_t s_bar;
+
+    const int b = blockIdx.x;
+    const int t = threadIdx.x;
+    const int warp = t >> 5, lane = t & 31;
+    const int n_q = p.n_q;
+    if (t == 0) {
+        mbar_init(&s_bar, 1);
+        fence_mbar_init();
+    }
+    griddep_wait();
+    if (t < n_q) {
+        s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
+        s_par[t] = t == 0 ? -1 : parent_of(p, b, t);
+    }
+    __syncthreads();
+
+    // every leaf: the number of accepted nodes from the root down its path
+    int key = -1;
+    if (t < n_q) {
+        bool leaf = true;
+        for (int c = t + 1; c < n_q; ++c)
+            if (s_par[c] == t) { leaf = false; break; }
+        if (leaf) {
+            int depth = 0;
+            for (int v = t; v != 0; v = s_par[v]) ++depth;
+            int len = depth, pos = depth;
+            for (int v = t; v != 0; v = s_par[v], --pos)
+                if (!s_acc[v]) len = pos - 1;
+            key = (len << 8) | (255 - t);   // most accepted, then smallest leaf
+        }
+    }
+    if (warp < 2) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+        if (lane == 0) s_key[warp] = key;
+    }
+    __syncthreads();
+    if (t == 0) {
+        const int best = max(s_key[0], s_key[1]);
+        const int best_len = best >> 8, best_leaf = 255 - (best & 255);
+        int nodes[kAcceptMaxNq];
+        int depth = 0;
+        for (int v = best_leaf; v != 0; v = s_par[v]) nodes[depth++] = v;
+        const int e = best_len > 0 ? nodes[depth - best_len] : 0;
+        p.n_accepted[b] = best_len;
+        if (p.path) {
+            for (int k = 0; k < n_q; ++k)
+                p.path[(int64_t)b * n_q + k] = k < best_len ? nodes[depth - 1 - k] : -1;
+        }
+        if (p.diag) {
+            for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
+        }
+        int has_children = 0;
+        for (int c = e + 1; c < n_q; ++c)
+            if (s_par[c] == e) { has_children = 1; break; }
+        s_e = e;
+        s_has_children = has_children;
+    }
+    __syncthreads();
+
+    // the slice that holds the inverse-CDF target, from the per-slice masses
+    const int e = s_e;
+    const int64_t row = (int64_t)b * n_q + e;
+    if (warp == 0) {
+        const float* mass = p.ws_mass + row * kAcceptMaxCluster * 2;
+        const float wc = lane < p.C ? mass[2 * lane] : 0.f;
+        const float pc = lane < p.C ? mass[2 * lane + 1] : 0.f;
+        const float wtot = warp_sum(wc);
+        const bool resid = s_has_children && wtot > 0.f;   // a residual without mass falls back to p
+        const float mc = resid ? wc : pc;
+        const float tot = resid ? wtot : warp_sum(pc);
+        const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
+        const float target = word_uniform(rnd.w[1]) * tot;
+        float incl = mc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const float excl = incl - mc;
+        const unsigned hit = __ballot_sync(0xffffffffu, mc > 0.f && incl > target);
+        const unsigned pos = __ballot_sync(0xffffffffu, mc > 0.f);
+        int owner = -1;
+        float tin = INFINITY;
+        if (hit) {
+            owner = __ffs(hit) - 1;
+            tin = target - __shfl_sync(0xffffffffu, excl, owner);
+        } else if (pos) {
+            owner = 31 - __clz(pos);   // rounding left the target past the end: last slice with mass
+        }
+        if (lane == 0) {
+            s_owner = owner;
+            s_tin = tin;
+            s_resid = resid ? 1 : 0;
+        }
+    }
+    __syncthreads();
+    const int owner = s_owner;
+    if (owner < 0) {   // no mass at all (degenerate input)
+        if (t == 0) p.next_token[b] = 0;
+        return;
+    }
+    const bool resid = s_resid != 0;
+    const float tin = s_tin;
+    const int64_t lo = (int64_t)owner * p.chunk;
+    int64_t n64 = (int64_t)p.V - lo;
+    if (n64 > p.chunk) n64 = p.chunk;
+    const int n = (int)n64;
+    const float* zr = p.z + row * p.V + lo;
+    const float* qr = p.q + row * p.V + lo;
     if (p.bulk) {
         if (t == 0) {
-            mbar_init(&sh.bar, 1);
-            fence_mbar_init();
+            mbar_arrive_expect_tx(&s_bar, (uint32_t)(n * 4 * (resid ? 2 : 1)));
+            bulk_g2s(sz, zr, (uint32_t)(n * 4), &s_bar);
+            if (resid) bulk_g2s(sq, qr, (uint32_t)(n * 4), &s_bar);
         }
-        __syncthreads();
-        if (t == 0) {
-            mbar_arrive_expect_tx(&sh.bar, (uint32_t)(n * 8));
-            if (n > 0) {
-                bulk_g2s(sz, zrow, (uint32_t)(n * 4), &sh.bar);
-                bulk_g2s(sq, qrow, (uint32_t)(n * 4), &sh.bar);
-            }
-        }
+        mbar_wait(&s_bar, 0u, p.err, 0x05000000u);
     } else {
-        for (int e = t; e < n; e += kNT) {
-            sz[e] = zrow[e];
-            sq[e] = qrow[e];
+        for (int k = t; k < n; k += kST) {
+            sz[k] = zr[k];
+            if (resid) sq[k] = qr[k];
         }
+        __syncthreads();
     }
-    // children of row j (nodes scored by this row)
-    if (t == 0) {
-        int nc = 0;
-        for (int c = j + 1; c < p.n_q; ++c)
-            if (parent_of(p, b, c) == j) sh.children[nc++] = c;
-        sh.n_children = nc;
+    // weights of the slice, in place
+    const float* sts = p.ws_stats + row * 4;
+    const float m1 = sts[0], inv_s1 = 1.f / sts[1], m2 = sts[2], inv_s2 = 1.f / sts[3];
+    const float thr = p.clamp ? 0.1f * inv_s2 : -1.0f;
+    for (int k = t; k < n; k += kST) {
+        const float x = sz[k] * p.invT;
+        const float pk = ex2((x - m1) * kLog2e) * inv_s1;
+        float w = pk;
+        if (resid) {
+            const float qk = sq[k];
+            const float a = fmaf(p.eta, qk - pk, x);
+            float ph = ex2((a - m2) * kLog2e) * inv_s2;
+            if (ph < thr) ph = pk;
+            w = fmaxf(fmaxf(pk - ph, pk - qk), 0.f);
+        }
+        sz[k] = w;
     }
-    if (p.bulk) mbar_wait(&sh.bar, 0, p.err);
     __syncthreads();
-    const bool has_children = sh.n_children > 0;
-
-    // ---- pass 1: p = softmax(z / T) -----------------------------------
-    float xr[E], er[E];
-    float m_t = -INFINITY;
+    // one contiguous segment per warp: its sum, then the warp whose segment holds the target
+    const int seg = (n + kSW * 32 - 1) / (kSW * 32) * 32;
+    const int g0 = warp * seg;
+    const int g1 = min(n, g0 + seg);
+    float acc = 0.f;
+    for (int k = g0 + lane; k < g1; k += 32) acc += sz[k];
+    acc = warp_sum(acc);
+    if (lane == 0) s_seg[warp] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        const float v = lane < kSW ? s_seg[lane] : 0.f;
+        float incl = v;
 #pragma unroll
-    for (int f = 0; f < F; ++f) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int el = 4 * (t + f * kNT) + c;
-            const float x = el < n ? sz[el] * p.invT : -INFINITY;
-            xr[4 * f + c] = x;
-            m_t = fmaxf(m_t, x);
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && incl > tin);
+        const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+        int ow = -1;
+        float tw = INFINITY;
+        if (hit) {
+            ow = __ffs(hit) - 1;
+            tw = tin - __shfl_sync(0xffffffffu, incl - v, ow);
+        } else if (pos) {
+            ow = 31 - __clz(pos);
+        }
+        if (lane == 0) {
+            s_ow = ow;
+            s_tw = tw;
         }
     }
-    float s_t = 0.f;
-#pragma unroll
-    for (int k = 0; k < E; ++k) {
-        er[k] = (xr[k] == -INFINITY) ? 0.f : exp2f((xr[k] - m_t) * kLog2e);
-        s_t += er[k];
+    __syncthreads();
+    const int ow = s_ow;
+    if (ow < 0) {   // the recomputed slice has no mass: first entry of the slice
+        if (t == 0) p.next_token[b] = (int)lo;
+        return;
     }
-    MS cta1 = block_ms(MS{m_t, s_t}, sh);
-    if (t == 0) sh.x_ms1 = cta1;
-    cluster.sync();
-    MS tot1 = MS{-INFINITY, 0.f};
-    for (int c = 0; c < C; ++c) tot1 = ms_combine(tot1, cluster.map_shared_rank(&sh, c)->x_ms1);
-    // p_k = er_k * f_t
-    const float f_t = (m_t == -INFINITY) ? 0.f : exp2f((m_t - tot1.m) * kLog2e) / tot1.s;
-
-    // ---- pass 2: p_hat = softmax(z/T + eta (q - p)) ----------------------
-    float m2_t = -INFINITY;
-#pragma unroll
-    for (int f = 0; f < F; ++f) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int k = 4 * f + c;
-            const int el = 4 * (t + f * kNT) + c;
-            if (el < n) {
-                const float pk = er[k] * f_t;
-                xr[k] = xr[k] + p.eta * (sq[el] - pk);
-            }
-            m2_t = fmaxf(m2_t, xr[k]);
-        }
-    }
-    float s2_t = 0.f;
-#pragma unroll
-    for (int k = 0; k < E; ++k) {
-        xr[k] = (xr[k] == -INFINITY) ? 0.f : exp2f((xr[k] - m2_t) * kLog2e);
-        s2_t += xr[k];
-    }
-    MS cta2 = block_ms(MS{m2_t, s2_t}, sh);
-    if (t == 0) sh.x_ms2 = cta2;
-    cluster.sync();
-    MS tot2 = MS{-INFINITY, 0.f};
-    for (int c = 0; c < C; ++c) tot2 = ms_combine(tot2, cluster.map_shared_rank(&sh, c)->x_ms2);
-    // p_hat_k = xr_k * g_t; max_k p_hat_k = 1 / s2 (the arg-max term is exp(0)).
-    const float g_t = (m2_t == -INFINITY) ? 0.f : exp2f((m2_t - tot2.m) * kLog2e) / tot2.s;
-    const float thr = p.clamp ? 0.1f * (1.0f / tot2.s) : -1.0f;
-
-    // ---- ratio test of every draft node scored by this row -------------
-    for (int ci = 0; ci < sh.n_children; ++ci) {
-        const int node = sh.children[ci];
-        const int tok = p.tokens[(int64_t)b * p.n_q + node];
-        const int64_t el = (int64_t)tok - lo;
-        if (tok < 0 || tok >= p.V || el < 0 || el >= n) continue;   // owner only
-        const int e4 = (int)el >> 2;
-        if ((e4 % kNT) != t) continue;
-        const int kk = 4 * (e4 / kNT) + ((int)el & 3);
-        float ek = 0.f, hk = 0.f;
-#pragma unroll
-        for (int k = 0; k < E; ++k)
-            if (k == kk) { ek = er[k]; hk = xr[k]; }
-        const float pt = ek * f_t;
-        float ph = hk * g_t;
-        if (ph < thr) ph = pt;
-        const float qt = sq[el];
-        const float ratio = (qt == 0.f) ? INFINITY : ph / qt;
-        const Philox4 rnd = philox4x32_10((uint32_t)node, (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
-        const float r = word_uniform(rnd.w[0]);
-        p.ws_accept[(int64_t)b * p.n_q + node] = (r <= fminf(1.0f, ratio)) ? 1 : 0;
-        if (p.diag) {
-            float* dg = p.diag + ((int64_t)b * p.n_q + node) * 5;
-            dg[0] = pt; dg[1] = ph; dg[2] = qt; dg[3] = ratio; dg[4] = r;
-        }
-    }
-    // Out-of-range draft tokens are rejected (memory-safe handling of bad input).
-    if (rank == 0 && t == 0) {
-        for (int ci = 0; ci < sh.n_children; ++ci) {
-            const int node = sh.children[ci];
-            const int tok = p.tokens[(int64_t)b * p.n_q + node];
-            if (tok < 0 || tok >= p.V) p.ws_accept[(int64_t)b * p.n_q + node] = 0;
-        }
-    }
-
-    if (t == 0) griddep_launch_dependents();
-
-    // ---- pass 3: candidate next token of this row ------------------------
-    const Philox4 rnd = philox4x32_10((uint32_t)(j + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
-    const float u = word_uniform(rnd.w[1]);
-    bool residual = has_children;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        float wsum[F];
-#pragma unroll
-        for (int f = 0; f < F; ++f) {
-            float acc = 0.f;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int k = 4 * f + c;
-                const int el = 4 * (t + f * kNT) + c;
-                float w = 0.f;
-                if (el < n) {
-                    const float pk = er[k] * f_t;
-                    if (residual) {
-                        float ph = xr[k] * g_t;
-                        if (ph < thr) ph = pk;
-                        w = fmaxf(fmaxf(pk - ph, pk - sq[el]), 0.f);
-                    } else {
-                        w = pk;
-                    }
-                }
-                acc += w;
-            }
-            wsum[f] = acc;
-        }
-        // stripe totals (stripe f = the f-th run of kNT float4s of this CTA)
-        const int warp = t >> 5, lane = t & 31;
-#pragma unroll
-        for (int f = 0; f < F; ++f) {
-            const float v = warp_sum(wsum[f]);
-            if (lane == 0) sh.red_f[warp][f] = v;
-        }
-        __syncthreads();
-        if (t < F) {
-            float s = 0.f;
-            for (int w = 0; w < kWarps; ++w) s += sh.red_f[w][t];
-            sh.stripe_total[t] = s;
-        }
-        __syncthreads();
-        float Wc = 0.f;
-        for (int f = 0; f < F; ++f) Wc += sh.stripe_total[f];
-        if (t == 0) sh.x_w = Wc;
-        cluster.sync();
-        float W = 0.f;
-        for (int c = 0; c < C; ++c) W += cluster.map_shared_rank(&sh, c)->x_w;
-        if (residual && !(W > 0.f)) {   // residual without mass: fall back to p
-            residual = false;
-            cluster.sync();             // peers done reading x_w before it is rewritten
-            continue;
-        }
-
-        // CTA level: first CTA whose running total passes u*W (else the last
-        // CTA with mass), and the target inside it.
-        const float target = u * W;
-        int owner = -1, last_pos = -1;
-        float cum = 0.f, t_in = INFINITY;
-        for (int c = 0; c < C; ++c) {
-            const float wc = cluster.map_shared_rank(&sh, c)->x_w;
-            if (wc > 0.f) {
-                last_pos = c;
-                if (owner < 0 && cum + wc > target) { owner = c; t_in = target - cum; }
-            }
-            cum += wc;
-        }
-        if (owner < 0) { owner = last_pos; t_in = INFINITY; }
-        if (owner == rank) {
-            // stripe level
-            int fs = -1, flast = -1;
-            float cs = 0.f, t_s = INFINITY;
-            for (int f = 0; f < F; ++f) {
-                const float v = sh.stripe_total[f];
-                if (v > 0.f) {
-                    flast = f;
-                    if (fs < 0 && cs + v > t_in) { fs = f; t_s = t_in - cs; }
-                }
-                cs += v;
-            }
-            if (fs < 0) { fs = flast; t_s = INFINITY; }
-            // thread level: exclusive scan of this stripe's per-thread sums
-            float v = 0.f;
-#pragma unroll
-            for (int f = 0; f < F; ++f)
-                if (f == fs) v = wsum[f];
+    if (warp == ow) {
+        const float tw = s_tw;
+        float ce = 0.f;
+        int kpick = -1, klast = -1;
+        for (int base = g0; base < g1; base += 32) {
+            const int k = base + lane;
+            const float v = k < g1 ? sz[k] : 0.f;
             float incl = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (lane == 31) sh.warp_tot[warp] = incl;
-            if (t == 0) { sh.pick_thread = kNT; sh.last_thread = -1; }
-            __syncthreads();
-            float woff = 0.f;
-            for (int w = 0; w < warp; ++w) woff += sh.warp_tot[w];
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 0.f;
-            excl += woff;
-            if (v > 0.f) {
-                atomicMax(&sh.last_thread, t);
-                if (excl + v > t_s) atomicMin(&sh.pick_thread, t);
+            const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && ce + incl > tw);
+            const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+            if (pos) klast = base + 31 - __clz(pos);
+            if (hit) {
+                kpick = base + __ffs(hit) - 1;
+                break;
             }
-            __syncthreads();
-            int pick = sh.pick_thread;
-            const bool fallback = (pick >= kNT);
-            if (fallback) pick = sh.last_thread;
-            if (t == pick && fs >= 0) {
-                // element level inside this thread's float4 of stripe fs
-                int kpick = -1, klast = -1;
-                float ce = excl;
-                const float t_e = fallback ? INFINITY : t_s;
-#pragma unroll
-                for (int f = 0; f < F; ++f) {
-                    if (f != fs) continue;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int k = 4 * f + c;
-                        const int el = 4 * (t + f * kNT) + c;
-                        float w = 0.f;
-                        if (el < n) {
-                            const float pk = er[k] * f_t;
-                            if (residual) {
-                                float ph = xr[k] * g_t;
-                                if (ph < thr) ph = pk;
-                                w = fmaxf(fmaxf(pk - ph, pk - sq[el]), 0.f);
-                            } else {
-                                w = pk;
-                            }
-                        }
-                        if (w > 0.f) {
-                            klast = c;
-                            if (kpick < 0 && ce + w > t_e) kpick = c;
-                        }
-                        ce += w;
-                    }
-                }
-                if (kpick < 0) kpick = klast;
-                if (kpick < 0) kpick = 0;   // unreachable: the stripe has mass
-                p.ws_sample[row] = (int)(lo + 4 * (t + fs * kNT) + kpick);
-            }
-            if (t == 0 && (pick < 0 || fs < 0)) p.ws_sample[row] = (int)lo;   // unreachable guard
+            ce += __shfl_sync(0xffffffffu, incl, 31);
         }
-        break;
-    }
-    // keep this CTA's shared memory alive until every peer has read it
-    cluster.sync();
-}
-
-// One thread per sequence: pick the winning path and the next token.
-__global__ void accept_select_kernel(const AcceptParams p) {
-    griddep_wait();
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= p.B) return;
-    const int n_q = p.n_q;
-    const int32_t* acc = p.ws_accept + (int64_t)b * n_q;
-    int n_children[kAcceptMaxNq];
-    for (int i = 0; i < n_q; ++i) n_children[i] = 0;
-    for (int i = 1; i < n_q; ++i) n_children[parent_of(p, b, i)]++;
-    int best_len = -1, best_leaf = 0;
-    for (int leaf = 0; leaf < n_q; ++leaf) {
-        if (n_children[leaf] != 0) continue;
-        int nodes[kAcceptMaxNq];
-        int depth = 0;
-        for (int v = leaf; v != 0; v = parent_of(p, b, v)) nodes[depth++] = v;
-        int len = 0;
-        while (len < depth && acc[nodes[depth - 1 - len]]) ++len;
-        if (len > best_len) { best_len = len; best_leaf = leaf; }
-    }
-    int nodes[kAcceptMaxNq];
-    int depth = 0;
-    for (int v = best_leaf; v != 0; v = parent_of(p, b, v)) nodes[depth++] = v;
-    const int e = best_len > 0 ? nodes[depth - best_len] : 0;
-    p.n_accepted[b] = best_len;
-    p.next_token[b] = p.ws_sample[(int64_t)b * n_q + e];
-    if (p.path) {
-        for (int k = 0; k < n_q; ++k)
-            p.path[(int64_t)b * n_q + k] = k < best_len ? nodes[depth - 1 - k] : -1;
-    }
-    if (p.diag) {
-        for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
+        if (kpick < 0) kpick = klast >= 0 ? klast : g0;
+        if (lane == 0) p.next_token[b] = (int)(lo + kpick);
     }
 }
 
 template <int F>
-cudaError_t launch_rows(const AcceptParams& p, int C, cudaStream_t st) {
+cudaError_t set_rows_attrs(int C, size_t smem) {
     auto kern = accept_rows_kernel<F>;
-    const size_t smem = (size_t)p.chunk * 8;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    if (C > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
+    if (C > 8) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+}
+
+size_t rows_smem(int groups, int nbuf) { return (size_t)nbuf * groups * 32; }
+
+template <int F>
+cudaError_t launch_rows(const AcceptParams& p, cudaStream_t st) {
+    const size_t smem = rows_smem(p.groups, p.nbuf);
+    cudaError_t e = set_rows_attrs<F>(p.C, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C, p.B * p.n_q, 1);
-    cfg.blockDim = dim3(kNT, 1, 1);
+    cfg.gridDim = dim3(p.nclusters * p.C, 1, 1);
+    cfg.blockDim = dim3(kRT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.x = p.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, accept_rows_kernel<F>, p);
 }
 
 template <int F>
-cudaError_t max_clusters(int C, int chunk, int* out) {
-    auto kern = accept_rows_kernel<F>;
-    const size_t smem = (size_t)chunk * 8;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+cudaError_t max_clusters(int C, size_t smem, int* out) {
+    cudaError_t e = set_rows_attrs<F>(C, smem);
     if (e != cudaSuccess) return e;
-    if (C > 8) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, 1, 1);
-    cfg.blockDim = dim3(kNT, 1, 1);
+    cfg.blockDim = dim3(kRT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -475,7 +879,7 @@ cudaError_t max_clusters(int C, int chunk, int* out) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaOccupancyMaxActiveClusters(out, kern, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, accept_rows_kernel<F>, &cfg);
 }
 
 #define RAPID_ACCEPT_DISPATCH(FN, F_, ...)             \
@@ -487,71 +891,108 @@ cudaError_t max_clusters(int C, int chunk, int* out) {
         case 5: return FN<5>(__VA_ARGS__);             \
         case 6: return FN<6>(__VA_ARGS__);             \
         case 7: return FN<7>(__VA_ARGS__);             \
-        case 8: return FN<8>(__VA_ARGS__);             \
-        case 9: return FN<9>(__VA_ARGS__);             \
-        case 10: return FN<10>(__VA_ARGS__);           \
-        case 11: return FN<11>(__VA_ARGS__);           \
-        case 12: return FN<12>(__VA_ARGS__);           \
-        case 13: return FN<13>(__VA_ARGS__);           \
-        case 14: return FN<14>(__VA_ARGS__);           \
-        case 15: return FN<15>(__VA_ARGS__);           \
-        case 16: return FN<16>(__VA_ARGS__);           \
         default: return cudaErrorNotSupported;         \
     }
 
-cudaError_t max_clusters_dispatch(int F, int C, int chunk, int* out) {
-    RAPID_ACCEPT_DISPATCH(max_clusters, F, C, chunk, out)
+cudaError_t max_clusters_dispatch(int F, int C, size_t smem, int* out) {
+    RAPID_ACCEPT_DISPATCH(max_clusters, F, C, smem, out)
 }
 
-cudaError_t launch_rows_dispatch(int F, const AcceptParams& p, int C, cudaStream_t st) {
-    RAPID_ACCEPT_DISPATCH(launch_rows, F, p, C, st)
+cudaError_t launch_rows_dispatch(int F, const AcceptParams& p, cudaStream_t st) {
+    RAPID_ACCEPT_DISPATCH(launch_rows, F, p, st)
+}
+
+AcceptShape shape_for(int V, int C) {
+    AcceptShape sh{};
+    sh.vocab = V;
+    sh.cluster = C;
+    sh.chunk = ((V + C - 1) / C + 3) / 4 * 4;
+    sh.groups = (sh.chunk / 4 + 31) / 32 * 32;
+    sh.F = (sh.groups + kGT - 1) / kGT;
+    sh.nbuf = kGroups;   // one resident row per warp group
+    return sh;
+}
+
+// Co-resident clusters per (device, F, C, shared memory), cached: the
+// occupancy query is not free.
+struct OccEntry {
+    int dev, F, C;
+    size_t smem;
+    int n;
+};
+std::mutex g_occ_mu;
+OccEntry g_occ[64];
+int g_nocc = 0;
+
+int occupancy(int dev, int F, int C, size_t smem) {
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mu);
+        for (int i = 0; i < g_nocc; ++i) {
+            const OccEntry& o = g_occ[i];
+            if (o.dev == dev && o.F == F && o.C == C && o.smem == smem) return o.n;
+        }
+    }
+    int n = 0;
+    if (max_clusters_dispatch(F, C, smem, &n) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    if (g_nocc < 64) g_occ[g_nocc++] = OccEntry{dev, F, C, smem, n};
+    return n;
 }
 
 }  // namespace
 
-AcceptShape accept_shape(int V, int preferred_cluster) {
-    AcceptShape sh{};
-    sh.vocab = V;
-    int C = (V + kNT * 32 - 1) / (kNT * 32);
-    if (preferred_cluster > 0) C = preferred_cluster;
-    if (C < 1) C = 1;
-    if (C > 16) C = 16;
-    for (;;) {
-        const int chunk = ((V + C - 1) / C + 3) / 4 * 4;
-        const int F = (chunk + 4 * kNT - 1) / (4 * kNT);
-        sh.cluster = C;
-        sh.chunk = chunk;
-        sh.F = F;
-        if (F <= 16 || C >= 16) break;
-        ++C;
-    }
-    return sh;
-}
-
-cudaError_t accept_check_cluster(AcceptShape* sh) {
-    // Shrink the cluster until the hardware can co-schedule one of it.
-    for (;;) {
-        int n = 0;
-        cudaError_t e = max_clusters_dispatch(sh->F, sh->cluster, sh->chunk, &n);
-        if (e == cudaSuccess && n > 0) return cudaSuccess;
-        (void)cudaGetLastError();
-        if (sh->cluster <= 1) return e == cudaSuccess ? cudaErrorNotSupported : e;
-        // next smaller power-of-two-ish size with the same row coverage
-        const int C = sh->cluster > 8 ? 8 : sh->cluster / 2;
-        sh->cluster = C;
-        sh->chunk = ((sh->vocab + C - 1) / C + 3) / 4 * 4;
-        sh->F = (sh->chunk + 4 * kNT - 1) / (4 * kNT);
-        if (sh->F > 16) return cudaErrorNotSupported;
-    }
-}
-
-cudaError_t launch_accept(const AcceptParams& p, const AcceptShape& sh, cudaStream_t st) {
-    cudaError_t e = launch_rows_dispatch(sh.F, p, sh.cluster, st);
+cudaError_t accept_plan(int V, int rows, AcceptShape* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int threads = 64;
+    int cmin = (V + kAcceptMaxSlice - 1) / kAcceptMaxSlice;
+    if (cmin < 1) cmin = 1;
+    int cmax = (V + kMinSlice - 1) / kMinSlice;
+    if (cmax > kAcceptMaxCluster) cmax = kAcceptMaxCluster;
+    if (cmax < cmin) cmax = cmin;
+    bool found = false;
+    int64_t best_cost = 0;
+    AcceptShape best{};
+    for (int C = cmin; C <= cmax && C <= kAcceptMaxCluster; ++C) {
+        AcceptShape sh = shape_for(V, C);
+        if (sh.F > kAcceptMaxF || rows_smem(sh.groups, sh.nbuf) > kSmemBudget) continue;
+        sh.max_clusters = occupancy(dev, sh.F, C, rows_smem(sh.groups, sh.nbuf));
+        if (sh.max_clusters <= 0) continue;
+        const int ncl = rows < sh.max_clusters ? rows : sh.max_clusters;
+        const int64_t cost = (int64_t)((rows + ncl - 1) / ncl) * sh.chunk;
+        if (!found || cost < best_cost || (cost == best_cost && sh.nbuf > best.nbuf)) {
+            found = true;
+            best_cost = cost;
+            best = sh;
+        }
+    }
+    if (!found) return cudaErrorNotSupported;
+    *out = best;
+    return cudaSuccess;
+}
+
+cudaError_t launch_accept(const AcceptParams& p0, const AcceptShape& sh, cudaStream_t st) {
+    AcceptParams p = p0;
+    p.C = sh.cluster;
+    p.chunk = sh.chunk;
+    p.groups = sh.groups;
+    p.nbuf = sh.nbuf;
+    p.rows = p.B * p.n_q;
+    p.nclusters = p.rows < sh.max_clusters ? p.rows : sh.max_clusters;
+    if (p.nclusters < 1) return cudaErrorNotSupported;
+    cudaError_t e = launch_rows_dispatch(sh.F, p, st);
+    if (e != cudaSuccess) return e;
+    const size_t sel_smem = (size_t)p.chunk * 8;
+    e = cudaFuncSetAttribute(accept_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sel_smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((p.B + threads - 1) / threads, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.gridDim = dim3(p.B, 1, 1);
+    cfg.blockDim = dim3(kST, 1, 1);
+    cfg.dynamicSmemBytes = sel_smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -162,7 +162,10 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
 
 size_t rapid_accept_workspace_size(int B, int n_q, int V) {
     if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return 0;
-    return align_up((size_t)B * n_q * sizeof(int32_t)) * 2;
+    const size_t rows = (size_t)B * n_q;
+    const size_t C = (size_t)kAcceptMaxCluster;
+    return align_up(rows * sizeof(int32_t)) + align_up(rows * 4 * sizeof(float)) +
+           align_up(rows * C * 2 * sizeof(float));
 }
 
 rapid_status rapid_accept(const float* z_target, const float* q_draft, const int32_t* draft_tokens,
@@ -181,17 +184,23 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft, const int
     if (workspace_bytes < need) return RAPID_ENOMEM;
     if (reinterpret_cast<uintptr_t>(workspace) & 15u) return RAPID_EINVAL;
 
-    AcceptShape sh = accept_shape(V, 0);
-    if (accept_check_cluster(&sh) != cudaSuccess) return RAPID_EUNSUPPORTED;
+    AcceptShape sh{};
+    if (accept_plan(V, B * n_q, &sh) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RAPID_EUNSUPPORTED;
+    }
 
+    const size_t rows = (size_t)B * n_q;
+    char* ws = static_cast<char*>(workspace);
     AcceptParams p{};
     p.z = z_target; p.q = q_draft; p.tokens = draft_tokens; p.parent = parent;
-    p.ws_accept = static_cast<int32_t*>(workspace);
-    p.ws_sample = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
-                                             align_up((size_t)B * n_q * sizeof(int32_t)));
+    p.ws_accept = reinterpret_cast<int32_t*>(ws);
+    ws += align_up(rows * sizeof(int32_t));
+    p.ws_stats = reinterpret_cast<float*>(ws);
+    ws += align_up(rows * 4 * sizeof(float));
+    p.ws_mass = reinterpret_cast<float*>(ws);
     p.diag = diag; p.n_accepted = n_accepted; p.next_token = next_token; p.path = path;
     p.B = B; p.n_q = n_q; p.V = V;
-    p.chunk = sh.chunk;
     p.bulk = ((V % 4) == 0 && aligned16(z_target) && aligned16(q_draft)) ? 1 : 0;
     p.clamp = (flags & RAPID_ACCEPT_TAIL_CLAMP) ? 1 : 0;
     p.invT = 1.0f / T;

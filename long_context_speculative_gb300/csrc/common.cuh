@@ -197,4 +197,10 @@ RAPID_DEVICE void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion to wait for).
+// src 16-byte aligned; bytes a multiple of 16.
+RAPID_DEVICE void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 }  // namespace rapid

@@ -20,7 +20,7 @@ RAPID_DTYPE_F32 = 0
 RAPID_DTYPE_BF16 = 1
 RAPID_ACCEPT_TAIL_CLAMP = 1
 RAPID_MAX_NQ = 64
-RAPID_MAX_VOCAB = 262144
+RAPID_MAX_VOCAB = 229376
 
 _lib = None
 

@@ -87,7 +87,7 @@ def test_small_tree_many_seeds():
         _run(w, 1.0, 1.0, seed, inp=inp)
 
 
-@pytest.mark.parametrize("V", [1, 3, 7, 1000, 1023, 1025, 4097, 65537, 262144])
+@pytest.mark.parametrize("V", [1, 3, 7, 1000, 1023, 1025, 4097, 65537, 229376])
 def test_vocab_sizes_and_unaligned_rows(V):
     w = wl.Workload("v", B=2, Hq=1, Hkv=1, d=64, n_q=4, prefix=1, layers=1, V=V, dtype="f32",
                     z_std=2.0, q_noise_std=1.0, q_noise_uses_T=True, seed=V)
@@ -128,7 +128,7 @@ def test_c_abi_rejects_bad_arguments():
     assert L.rapid_accept(*args) == 0
     torch.cuda.synchronize()
     for idx, val, code in [(7, 0.0, -1), (7, float("nan"), -1), (8, -1.0, -1), (5, 65, -1),
-                           (6, 0, -1), (6, 262145, -1), (10, 2, -1), (16, 4, -3), (0, None, -1)]:
+                           (6, 0, -1), (6, 229377, -1), (10, 2, -1), (16, 4, -3), (0, None, -1)]:
         bad = list(args)
         bad[idx] = val
         assert L.rapid_accept(*bad) == code, (idx, val)
