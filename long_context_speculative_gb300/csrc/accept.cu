@@ -618,11 +618,13 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
     extern __shared__ float4 sel_dyn[];
     float* sz = reinterpret_cast<float*>(sel_dyn);   // [chunk] z of the slice, then its weights
     float* sq = sz + p.chunk;                        // [chunk] q of the slice
-    __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq];
+    __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq], s_kids[kAcceptMaxNq];
     __shared__ int s_key[2];
     __shared__ int s_e, s_has_children, s_resid, s_owner, s_ow;
     __shared__ float s_tin, s_tw;
     __shared__ float s_seg[kSW];
+    __shared__ float2 s_mass[kAcceptMaxNq][kAcceptMaxCluster];   // every row's slice masses
+    __shared__ float4 s_stats[kAcceptMaxNq];
     __shared__ __align__(8) uint64_t s_bar;
 
     const int b = blockIdx.x;
@@ -637,16 +639,23 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
     if (t < n_q) {
         s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
         s_par[t] = t == 0 ? -1 : parent_of(p, b, t);
+        s_kids[t] = 0;
+        s_stats[t] = reinterpret_cast<const float4*>(p.ws_stats)[(int64_t)b * n_q + t];
     }
+    // the per-slice masses and statistics of every row of the sequence, loaded
+    // while the path is chosen
+    for (int x = t; x < n_q * p.C; x += kST) {
+        const int r = x / p.C, cc = x - r * p.C;
+        s_mass[r][cc] = reinterpret_cast<const float2*>(p.ws_mass)[((int64_t)b * n_q + r) * kAcceptMaxCluster + cc];
+    }
+    __syncthreads();
+    if (t > 0 && t < n_q) s_kids[s_par[t]] = 1;   // every writer stores the same value
     __syncthreads();
 
     // every leaf: the number of accepted nodes from the root down its path
     int key = -1;
     if (t < n_q) {
-        bool leaf = true;
-        for (int c = t + 1; c < n_q; ++c)
-            if (s_par[c] == t) { leaf = false; break; }
-        if (leaf) {
+        if (!s_kids[t]) {   // a leaf
             int depth = 0;
             for (int v = t; v != 0; v = s_par[v]) ++depth;
             int len = depth, pos = depth;
@@ -676,11 +685,8 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
         if (p.diag) {
             for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
         }
-        int has_children = 0;
-        for (int c = e + 1; c < n_q; ++c)
-            if (s_par[c] == e) { has_children = 1; break; }
         s_e = e;
-        s_has_children = has_children;
+        s_has_children = s_kids[e];
     }
     __syncthreads();
 
@@ -688,9 +694,8 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
     const int e = s_e;
     const int64_t row = (int64_t)b * n_q + e;
     if (warp == 0) {
-        const float* mass = p.ws_mass + row * kAcceptMaxCluster * 2;
-        const float wc = lane < p.C ? mass[2 * lane] : 0.f;
-        const float pc = lane < p.C ? mass[2 * lane + 1] : 0.f;
+        const float wc = lane < p.C ? s_mass[e][lane].x : 0.f;
+        const float pc = lane < p.C ? s_mass[e][lane].y : 0.f;
         const float wtot = warp_sum(wc);
         const bool resid = s_has_children && wtot > 0.f;   // a residual without mass falls back to p
         const float mc = resid ? wc : pc;
@@ -749,9 +754,10 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
         __syncthreads();
     }
     // weights of the slice, in place
-    const float* sts = p.ws_stats + row * 4;
-    const float m1 = sts[0], inv_s1 = 1.f / sts[1], m2 = sts[2], inv_s2 = 1.f / sts[3];
+    const float4 sts = s_stats[e];
+    const float m1 = sts.x, inv_s1 = 1.f / sts.y, m2 = sts.z, inv_s2 = 1.f / sts.w;
     const float thr = p.clamp ? 0.1f * inv_s2 : -1.0f;
+#pragma unroll 4
     for (int k = t; k < n; k += kST) {
         const float x = sz[k] * p.invT;
         const float pk = ex2((x - m1) * kLog2e) * inv_s1;
@@ -805,29 +811,49 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
         return;
     }
     if (warp == ow) {
+        // the segment in 32 contiguous runs, one per lane: run sums, the run
+        // that holds the target, then a sequential scan of that run
         const float tw = s_tw;
-        float ce = 0.f;
-        int kpick = -1, klast = -1;
-        for (int base = g0; base < g1; base += 32) {
-            const int k = base + lane;
-            const float v = k < g1 ? sz[k] : 0.f;
-            float incl = v;
+        const int per = (g1 - g0 + 31) / 32;
+        const int a0 = min(g1, g0 + lane * per);
+        const int a1 = min(g1, a0 + per);
+        float ls = 0.f;
+        for (int k = a0; k < a1; ++k) ls += sz[k];
+        float incl = ls;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && ce + incl > tw);
-            const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
-            if (pos) klast = base + 31 - __clz(pos);
-            if (hit) {
-                kpick = base + __ffs(hit) - 1;
-                break;
-            }
-            ce += __shfl_sync(0xffffffffu, incl, 31);
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        if (kpick < 0) kpick = klast >= 0 ? klast : g0;
-        if (lane == 0) p.next_token[b] = (int)(lo + kpick);
+        const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > tw);
+        const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
+        int run = -1;
+        float tl = INFINITY;
+        if (hit) {
+            run = __ffs(hit) - 1;
+            tl = tw - __shfl_sync(0xffffffffu, incl - ls, run);
+        } else if (pos) {
+            run = 31 - __clz(pos);
+        }
+        if (lane == run) {
+            float ce = 0.f;
+            int kpick = -1, klast = -1;
+            for (int k = a0; k < a1; ++k) {
+                const float w = sz[k];
+                if (w > 0.f) {
+                    klast = k;
+                    if (ce + w > tl) {
+                        kpick = k;
+                        break;
+                    }
+                }
+                ce += w;
+            }
+            if (kpick < 0) kpick = klast;
+            p.next_token[b] = (int)(lo + kpick);
+        } else if (run < 0 && lane == 0) {
+            p.next_token[b] = (int)(lo + g0);   // unreachable: the segment has mass
+        }
     }
 }
 
