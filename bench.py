@@ -27,7 +27,8 @@ METRIC = "verify-step KV-cache HBM GB/s vs GB300 peak; verify steps/s at 120K co
 UNIT = "verify_steps/s"
 WORKLOAD = "llama3.1-8b_32layers_120k"
 SRC_FILES_TRAFFIC = ["long_context_speculative_gb300/csrc/attn_tc.cu",
-                     "long_context_speculative_gb300/csrc/attn_simt.cu"]
+                     "long_context_speculative_gb300/csrc/attn_simt.cu",
+                     "long_context_speculative_gb300/csrc/attn.cuh"]
 
 
 def _dist_env():
@@ -418,6 +419,26 @@ def accept_batch_roofline(w, dev, stream, reps=20):
             "avg_launch_ms": ms, "peak_source": src + " (hbm_gbs, copy)"}
 
 
+def profile_accept(w, B):
+    """Three rapid_accept calls on B sequences of w (chain or tree as w is), no timing."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    inp = wl.accept_inputs(w, B=B)
+    dev = torch.device("cuda:0")
+    z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
+    par = None if inp.parent is None else inp.parent.to(dev)
+    for i in range(3):
+        rapid.accept(z, q, tok, par, T=w.T, eta=w.eta, seed=i)
+    torch.cuda.synchronize()
+    err = rapid.rapid_device_error()
+    print(json.dumps({"profile_accept": B, "rows": B * w.n_q, "vocab": w.V, "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -427,6 +448,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="named workload (default: the 32-layer 120K Llama-3.1-8B step)")
+    ap.add_argument("--profile-accept", type=int, default=0, metavar="B",
+                    help="only run rapid_accept three times on B sequences of the "
+                         "workload's rows (a fixed launch sequence for ncu captures)")
     args = ap.parse_args()
     from long_context_speculative_gb300 import workloads as wl
     w = wl.LLAMA8B_120K
@@ -434,7 +458,9 @@ def main():
         w = {x.name: x for x in wl.ALL}[args.workload]
     global WORKLOAD
     WORKLOAD = w.name
-    if args.impl == "reference":
+    if args.profile_accept > 0:
+        profile_accept(w, args.profile_accept)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_gpu(args, w)
