@@ -389,7 +389,7 @@ def accept_batch_roofline(w, dev, stream, reps=20):
     from long_context_speculative_gb300 import rapid
     from long_context_speculative_gb300 import workloads as wl
 
-    Bb = max(1, -(-100_000_000 // (w.n_q * w.V * 8)))
+    Bb = 16   # 16 independent sequences of the workload's rows: > 100 MB, > L2
     inp = wl.accept_inputs(w, B=Bb, parents=None if not w.tree else None)
     z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
     par = None if inp.parent is None else inp.parent.to(dev)

@@ -129,8 +129,8 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
 /* Acceptance                                                                */
 /* ------------------------------------------------------------------------ */
 
-/* Bytes of scratch that rapid_accept needs (at most 148 per node of the
- * B * n_q nodes, plus alignment); 0 for rejected sizes. */
+/* Bytes of scratch that rapid_accept needs (20 per node of the B * n_q nodes,
+ * plus alignment); 0 for rejected sizes. */
 size_t rapid_accept_workspace_size(int B, int n_q, int V);
 
 /*
@@ -196,7 +196,7 @@ enum { RAPID_NOALLOC_MAX_NODES = 4096 };
  * point; it computes exactly what rapid_accept computes, with the same
  * arguments and outputs.
  *
- * Scratch: a statically allocated device array of 592 KB inside librapid.so,
+ * Scratch: a statically allocated device array of 80 KB inside librapid.so,
  * held by every GPU that loads the library until the process exits.  It fits
  * B * n_q <= RAPID_NOALLOC_MAX_NODES; larger sizes return RAPID_EUNSUPPORTED.
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library

@@ -10,20 +10,17 @@
 //
 // Layout of the work.  A row of V entries is cut into C slices, one per CTA
 // of a thread-block cluster; the clusters are persistent and cluster c takes
-// rows c, c + nclusters, ...  Each CTA keeps its slice of the next rows'
-// (z, q) in shared memory through a ring of bulk (TMA) copies, so the next
-// rows stream in while the current one is worked on.  A row needs two
+// rows c, c + nclusters, ...  Each CTA keeps its slice of a row's (z, q) in
+// shared memory, filled by bulk (TMA) copies.  A row needs two
 // vocabulary-wide reductions -- the softmax of z/T and the softmax of the
 // augmented logits -- which every CTA completes from the C slice partials
 // that its peers send it with st.async into its shared memory (completion on
-// an mbarrier, double-buffered by row parity).  Two rows are in flight per
-// CTA: while the partials of row i travel, the CTA finishes row i - 1: the
-// ratio tests of the draft nodes scored by that row, and the row's residual
-// mass per slice (its p mass per slice follows from the first reduction).
-// The selection kernel then walks the chain or tree, picks n_accepted, and
-// draws the next token from the one row it needs: it finds the slice that
-// holds the inverse-CDF target from the per-slice masses and scans only that
-// slice.
+// an mbarrier).  Each CTA runs two warp groups on alternate rows, half a row
+// apart, so that one computes while the other waits on the cluster; a row's
+// buffer is refilled as soon as its second pass is done.  The rows kernel
+// leaves the ratio-test outcomes and each row's softmax statistics; the
+// selection kernel (one cluster per sequence) walks the chain or tree, picks
+// n_accepted, and draws the next token from the one row it needs.
 //
 // Exponentials are taken against one reference per warp: the warp's max of x
 // for p, and for the augmented logits a = x + eta (q - p) the bound
@@ -77,11 +74,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
     return unpack2(d);
 }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
-    return unpack2(d);
-}
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
@@ -123,15 +115,14 @@ struct RowsShared {
     uint64_t full[kGroups];   // the group's (z, q) slice landed
     uint64_t mb1[kGroups];    // slice partials of reduction 1 received
     uint64_t mb2[kGroups];    // slice partials of reduction 2 received
+    uint64_t stagger;         // group 0 is past its first reduction 1: group 1 may start
     float2 recv1[kGroups][kAcceptMaxCluster];   // (m, s) of x per slice
     float2 recv2[kGroups][kAcceptMaxCluster];   // (reference, s) of a per slice
     float recv2a[kGroups][kAcceptMaxCluster];   // max of a per slice
     float2 red1[kGroups][kGW];   // per-warp partials of the group's row
     float2 red2[kGroups][kGW];
     float red2a[kGroups][kGW];
-    float red3[kGroups][kGW];
-    float2 part1[kGroups];       // this slice's (m, s) of x
-    int arrived[kGroups][3];     // warps of the group done with pass 1, pass 2, the finish
+    int arrived[kGroups][2];     // warps of the group done with pass 1, pass 2
     int abort;                   // a wait gave up: stop waiting, let the kernel run out
 };
 
@@ -209,7 +200,6 @@ struct RowState {
     float e[4 * F];   // exp(x - mw) of this thread's entries (x = z / T)
     float mw;         // warp max of x
     float fw;         // exp(mw - m1) / s1: p = e * fw
-    float rw;         // warp reference of the augmented logits
     float m1, s1;     // row softmax statistics of x (after reduction 1)
 };
 
@@ -261,11 +251,10 @@ __device__ __forceinline__ MS pass1(RowState<F>& st, const float* zb, int G, flo
     return MS{mw, warp_sum(s.x + s.y)};
 }
 
-// Pass 2: p = e * fw; a = x + eta (q - p); h = exp(a - rw) stored over z in
-// shared memory (-inf past the slice end n, which keeps the padding intact);
-// the warp's (rw, sum) and its max of a.
+// Pass 2: p = e * fw; a = x + eta (q - p); the warp's (rw, sum of exp(a - rw))
+// and its max of a.
 template <int F>
-__device__ __forceinline__ MS pass2(RowState<F>& st, float* zb, const float* qb, int G, int n,
+__device__ __forceinline__ MS pass2(RowState<F>& st, const float* zb, const float* qb, int G,
                                     float invT, float eta, float* amax_w) {
     const int t = threadIdx.x % kGT;
     const float fw = st.mw == -INFINITY ? 0.f : ex2((st.mw - st.m1) * kLog2e) / st.s1;
@@ -315,21 +304,12 @@ __device__ __forceinline__ MS pass2(RowState<F>& st, float* zb, const float* qb,
             amax = max3(amax, a23.x, a23.y);
             const float2 g01 = fma2(a01, l2, nb);
             const float2 g23 = fma2(a23, l2, nb);
-            float4 h = make_float4(ex2(g01.x), ex2(g01.y), ex2(g23.x), ex2(g23.y));
             // same pairing and order of additions as pass 1, so that eta = 0
             // gives p_hat == p bit for bit
-            s = add2(s, make_float2(h.x, h.y));
-            s = add2(s, make_float2(h.z, h.w));
-            if (el + 4 > n) {
-                if (el >= n) h.x = -INFINITY;
-                if (el + 1 >= n) h.y = -INFINITY;
-                if (el + 2 >= n) h.z = -INFINITY;
-                h.w = -INFINITY;
-            }
-            *reinterpret_cast<float4*>(zb + el) = h;
+            s = add2(s, make_float2(ex2(g01.x), ex2(g01.y)));
+            s = add2(s, make_float2(ex2(g23.x), ex2(g23.y)));
         }
     }
-    st.rw = rw;
     *amax_w = redux_max(amax);
     return MS{rw, warp_sum(s.x + s.y)};
 }
@@ -364,8 +344,9 @@ accept_rows_kernel(const AcceptParams p) {
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.mb1[i], 1);
             mbar_init(&sh.mb2[i], 1);
-            sh.arrived[i][0] = sh.arrived[i][1] = sh.arrived[i][2] = 0;
+            sh.arrived[i][0] = sh.arrived[i][1] = 0;
         }
+        mbar_init(&sh.stagger, 1);
         sh.abort = 0;
         fence_mbar_init();
     }
@@ -438,6 +419,10 @@ accept_rows_kernel(const AcceptParams p) {
         }
         const int my_tok = pf_tok, my_par = pf_par;
         prefetch_node(i + 2);
+        // the groups run half a row apart, so that one computes while the
+        // other waits on the cluster
+        if (g == 1 && k == 0)
+            wait_or_abort(&sh.stagger, 0u, &sh.abort, p.err, 0x06000000u);
         if (p.bulk) {
             wait_or_abort(&sh.full[g], (uint32_t)(k & 1), &sh.abort, p.err,
                           0x01000000u | (unsigned)(i & 0xffff));
@@ -467,11 +452,6 @@ accept_rows_kernel(const AcceptParams p) {
             if (group_arrive(&sh.arrived[g][0])) {
                 const float2 x = lane < kGW ? sh.red1[g][lane] : make_float2(-INFINITY, 0.f);
                 const MS c1 = warp_ms(MS{x.x, x.y});
-                if (lane == 0) {   // read back after reduction 1 completes, which this send is part of
-                    sh.part1[g] = make_float2(c1.m, c1.s);
-                    __threadfence_block();
-                }
-                __syncwarp();
                 if (lane < C)
                     st_async_v2(mapa_u32(smem_u32(&sh.recv1[g][rank]), (uint32_t)lane), c1.m, c1.s,
                                 mapa_u32(smem_u32(&sh.mb1[g]), (uint32_t)lane));
@@ -492,10 +472,11 @@ accept_rows_kernel(const AcceptParams p) {
             st.m1 = r1.m;
             st.s1 = r1.s;
         }
+        if (g == 0 && k == 0 && tg == 0) mbar_arrive(&sh.stagger);
         // pass 2; the group's last warp sends the slice's (reference, s, max a)
         {
             float amw;
-            const MS w2 = pass2<F>(st, zb, qb, G, n, p.invT, p.eta, &amw);
+            const MS w2 = pass2<F>(st, zb, qb, G, p.invT, p.eta, &amw);
             if (lane == 0) {
                 sh.red2[g][wg] = make_float2(w2.m, w2.s);
                 sh.red2a[g][wg] = amw;
@@ -509,10 +490,11 @@ accept_rows_kernel(const AcceptParams p) {
                     st_async_v2(mapa_u32(smem_u32(&sh.recv2[g][rank]), (uint32_t)lane), c2.m, c2.s, rbar);
                     st_async_f32(mapa_u32(smem_u32(&sh.recv2a[g][rank]), (uint32_t)lane), ac, rbar);
                 }
-                if (lane == 0) {   // p mass of this slice
-                    const float2 c1 = sh.part1[g];
-                    p.ws_mass[(row * kAcceptMaxCluster + rank) * 2 + 1] =
-                        c1.y > 0.f ? c1.y * ex2((c1.x - st.m1) * kLog2e) / st.s1 : 0.f;
+                if (lane == 0 && p.bulk && i + 2 < nrows) {
+                    // every warp of the group is done with the buffer: it takes
+                    // the group's next row while reduction 2 travels
+                    fence_proxy_async_smem();
+                    load_row(i + 2);
                 }
             }
         }
@@ -550,49 +532,9 @@ accept_rows_kernel(const AcceptParams p) {
         } else if (key == -2) {
             p.ws_accept[node] = 0;   // token outside the vocabulary: reject
         }
-        // residual mass of the slice
-        const float gw = st.rw == -INFINITY ? 0.f : ex2((st.rw - m2) * kLog2e) / s2;
-        const float2 fw2 = make_float2(st.fw, st.fw), gw2 = make_float2(gw, gw);
-        float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int f = 0; f < F; ++f) {
-            if (group_valid<F>(f, G)) {
-                const int el = 4 * (tg + f * kGT);
-                const float4 h4 = *reinterpret_cast<const float4*>(zb + el);
-                const float4 q4 = *reinterpret_cast<const float4*>(qb + el);
-                const float2 p01 = mul2(make_float2(st.e[4 * f], st.e[4 * f + 1]), fw2);
-                const float2 p23 = mul2(make_float2(st.e[4 * f + 2], st.e[4 * f + 3]), fw2);
-                float2 h01 = mul2(make_float2(h4.x, h4.y), gw2);
-                float2 h23 = mul2(make_float2(h4.z, h4.w), gw2);
-                if (h01.x < thr) h01.x = p01.x;
-                if (h01.y < thr) h01.y = p01.y;
-                if (h23.x < thr) h23.x = p23.x;
-                if (h23.y < thr) h23.y = p23.y;
-                // max(p - p_hat, p - q, 0) = p - min(p, p_hat, q); padding
-                // (h = -inf, q = 0, p = 0) gives 0, min3 drops the NaN of -inf * 0
-                const float2 m01 = make_float2(min3(p01.x, h01.x, q4.x), min3(p01.y, h01.y, q4.y));
-                const float2 m23 = make_float2(min3(p23.x, h23.x, q4.z), min3(p23.y, h23.y, q4.w));
-                acc = add2(acc, sub2(p01, m01));
-                acc = add2(acc, sub2(p23, m23));
-            }
-        }
-        const float wsum = warp_sum(acc.x + acc.y);
-        if (lane == 0) sh.red3[g][wg] = wsum;
-        if (group_arrive(&sh.arrived[g][2])) {
-            // every warp of the group is done with the buffer
-            const float tot = warp_sum(lane < kGW ? sh.red3[g][lane] : 0.f);
-            if (lane == 0) {
-                p.ws_mass[(row * kAcceptMaxCluster + rank) * 2] = tot;
-                if (rank == 0) {
-                    float* sts = p.ws_stats + row * 4;
-                    sts[0] = st.m1; sts[1] = st.s1; sts[2] = m2; sts[3] = s2;
-                }
-                // the group's buffer takes its next row
-                if (p.bulk && i + 2 < nrows) {
-                    fence_proxy_async_smem();
-                    load_row(i + 2);
-                }
-            }
+        if (rank == 0 && tg == 0) {
+            float* sts = p.ws_stats + row * 4;
+            sts[0] = st.m1; sts[1] = st.s1; sts[2] = m2; sts[3] = s2;
         }
         if (!p.bulk) group_sync(g);   // the synchronous copy of the next row overwrites the buffer
     }
@@ -611,42 +553,46 @@ accept_rows_kernel(const AcceptParams p) {
     cluster.sync();
 }
 
-// One CTA per sequence: pick the winning path, then draw the next token from
-// row e (the last accepted node) by inverse CDF in token-id order with u_{e+1}:
-// the residual if e has children, else p (the bonus draw).
-__global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p) {
+// Selection, one thread-block cluster per sequence b, one CTA per vocabulary
+// slice.  Every CTA picks the winning path (from a few hundred bytes) and
+// the last accepted node e, then weights its slice of row e for the draw of
+// the next token by inverse CDF in token-id order with u_{e+1}: the residual
+// max(p - p_hat, p - q, 0) if e has children (a rejection happened below it),
+// else p (the bonus draw; also the fallback when the residual has no mass).
+// The weights stay in the CTA's shared memory; the slice totals cross the
+// cluster through distributed shared memory, and the CTA whose slice holds
+// the target scans it there.
+__device__ __forceinline__ float resid_weight(float z, float qk, float invT, float eta, float m1,
+                                              float inv_s1, float m2, float inv_s2, float thr) {
+    const float x = z * invT;
+    const float pk = ex2((x - m1) * kLog2e) * inv_s1;
+    const float a = fmaf(eta, qk - pk, x);
+    float ph = ex2((a - m2) * kLog2e) * inv_s2;
+    if (ph < thr) ph = pk;
+    return pk - min3(pk, ph, qk);   // max(p - p_hat, p - q, 0)
+}
+
+__global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParams p) {
+    cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ float4 sel_dyn[];
-    float* sz = reinterpret_cast<float*>(sel_dyn);   // [chunk] z of the slice, then its weights
-    float* sq = sz + p.chunk;                        // [chunk] q of the slice
+    float* sw = reinterpret_cast<float*>(sel_dyn);   // [chunk] weights of this slice
     __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq], s_kids[kAcceptMaxNq];
     __shared__ int s_key[2];
-    __shared__ int s_e, s_has_children, s_resid, s_owner, s_ow;
+    __shared__ int s_e, s_has_children, s_owner, s_ow;
     __shared__ float s_tin, s_tw;
     __shared__ float s_seg[kSW];
-    __shared__ float2 s_mass[kAcceptMaxNq][kAcceptMaxCluster];   // every row's slice masses
-    __shared__ float4 s_stats[kAcceptMaxNq];
-    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ float s_total[2];   // this slice's weight total; the cluster's
 
-    const int b = blockIdx.x;
+    const int cs = (int)cluster.block_rank();   // vocabulary slice
+    const int b = blockIdx.y;
     const int t = threadIdx.x;
     const int warp = t >> 5, lane = t & 31;
     const int n_q = p.n_q;
-    if (t == 0) {
-        mbar_init(&s_bar, 1);
-        fence_mbar_init();
-    }
     griddep_wait();
     if (t < n_q) {
         s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
         s_par[t] = t == 0 ? -1 : parent_of(p, b, t);
         s_kids[t] = 0;
-        s_stats[t] = reinterpret_cast<const float4*>(p.ws_stats)[(int64_t)b * n_q + t];
-    }
-    // the per-slice masses and statistics of every row of the sequence, loaded
-    // while the path is chosen
-    for (int x = t; x < n_q * p.C; x += kST) {
-        const int r = x / p.C, cc = x - r * p.C;
-        s_mass[r][cc] = reinterpret_cast<const float2*>(p.ws_mass)[((int64_t)b * n_q + r) * kAcceptMaxCluster + cc];
     }
     __syncthreads();
     if (t > 0 && t < n_q) s_kids[s_par[t]] = 1;   // every writer stores the same value
@@ -677,107 +623,124 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
         int depth = 0;
         for (int v = best_leaf; v != 0; v = s_par[v]) nodes[depth++] = v;
         const int e = best_len > 0 ? nodes[depth - best_len] : 0;
-        p.n_accepted[b] = best_len;
-        if (p.path) {
-            for (int k = 0; k < n_q; ++k)
-                p.path[(int64_t)b * n_q + k] = k < best_len ? nodes[depth - 1 - k] : -1;
-        }
-        if (p.diag) {
-            for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
+        if (cs == 0) {
+            p.n_accepted[b] = best_len;
+            if (p.path) {
+                for (int k = 0; k < n_q; ++k)
+                    p.path[(int64_t)b * n_q + k] = k < best_len ? nodes[depth - 1 - k] : -1;
+            }
+            if (p.diag) {
+                for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
+            }
         }
         s_e = e;
         s_has_children = s_kids[e];
     }
     __syncthreads();
 
-    // the slice that holds the inverse-CDF target, from the per-slice masses
     const int e = s_e;
     const int64_t row = (int64_t)b * n_q + e;
-    if (warp == 0) {
-        const float wc = lane < p.C ? s_mass[e][lane].x : 0.f;
-        const float pc = lane < p.C ? s_mass[e][lane].y : 0.f;
-        const float wtot = warp_sum(wc);
-        const bool resid = s_has_children && wtot > 0.f;   // a residual without mass falls back to p
-        const float mc = resid ? wc : pc;
-        const float tot = resid ? wtot : warp_sum(pc);
-        const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
-        const float target = word_uniform(rnd.w[1]) * tot;
-        float incl = mc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const float excl = incl - mc;
-        const unsigned hit = __ballot_sync(0xffffffffu, mc > 0.f && incl > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, mc > 0.f);
-        int owner = -1;
-        float tin = INFINITY;
-        if (hit) {
-            owner = __ffs(hit) - 1;
-            tin = target - __shfl_sync(0xffffffffu, excl, owner);
-        } else if (pos) {
-            owner = 31 - __clz(pos);   // rounding left the target past the end: last slice with mass
-        }
-        if (lane == 0) {
-            s_owner = owner;
-            s_tin = tin;
-            s_resid = resid ? 1 : 0;
-        }
-    }
-    __syncthreads();
-    const int owner = s_owner;
-    if (owner < 0) {   // no mass at all (degenerate input)
-        if (t == 0) p.next_token[b] = 0;
-        return;
-    }
-    const bool resid = s_resid != 0;
-    const float tin = s_tin;
-    const int64_t lo = (int64_t)owner * p.chunk;
+    const float4 sts = reinterpret_cast<const float4*>(p.ws_stats)[row];
+    const float m1 = sts.x, inv_s1 = 1.f / sts.y, m2 = sts.z, inv_s2 = 1.f / sts.w;
+    const float thr = p.clamp ? 0.1f * inv_s2 : -1.0f;   // max p_hat = 1 / s2
+    const int64_t lo = (int64_t)cs * p.chunk;
     int64_t n64 = (int64_t)p.V - lo;
     if (n64 > p.chunk) n64 = p.chunk;
-    const int n = (int)n64;
+    const int n = n64 > 0 ? (int)n64 : 0;
     const float* zr = p.z + row * p.V + lo;
     const float* qr = p.q + row * p.V + lo;
-    if (p.bulk) {
-        if (t == 0) {
-            mbar_arrive_expect_tx(&s_bar, (uint32_t)(n * 4 * (resid ? 2 : 1)));
-            bulk_g2s(sz, zr, (uint32_t)(n * 4), &s_bar);
-            if (resid) bulk_g2s(sq, qr, (uint32_t)(n * 4), &s_bar);
-        }
-        mbar_wait(&s_bar, 0u, p.err, 0x05000000u);
-    } else {
-        for (int k = t; k < n; k += kST) {
-            sz[k] = zr[k];
-            if (resid) sq[k] = qr[k];
-        }
-        __syncthreads();
-    }
-    // weights of the slice, in place
-    const float4 sts = s_stats[e];
-    const float m1 = sts.x, inv_s1 = 1.f / sts.y, m2 = sts.z, inv_s2 = 1.f / sts.w;
-    const float thr = p.clamp ? 0.1f * inv_s2 : -1.0f;
+
+    // The residual if e has children, else p; p also when the residual has no
+    // mass in any slice.
+    bool resid = s_has_children != 0;
+    for (;;) {
+        float acc = 0.f;
+        if (p.bulk) {   // 16-byte aligned rows, n a multiple of 4
+            const float4* z4 = reinterpret_cast<const float4*>(zr);
+            const float4* q4 = reinterpret_cast<const float4*>(qr);
+            float4* w4 = reinterpret_cast<float4*>(sw);
+#pragma unroll 2
+            for (int k = t; k < n / 4; k += kST) {
+                const float4 a = z4[k];
+                float4 w;
+                if (resid) {
+                    const float4 c = q4[k];
+                    w.x = resid_weight(a.x, c.x, p.invT, p.eta, m1, inv_s1, m2, inv_s2, thr);
+                    w.y = resid_weight(a.y, c.y, p.invT, p.eta, m1, inv_s1, m2, inv_s2, thr);
+                    w.z = resid_weight(a.z, c.z, p.invT, p.eta, m1, inv_s1, m2, inv_s2, thr);
+                    w.w = resid_weight(a.w, c.w, p.invT, p.eta, m1, inv_s1, m2, inv_s2, thr);
+                } else {
+                    w.x = ex2((a.x * p.invT - m1) * kLog2e) * inv_s1;
+                    w.y = ex2((a.y * p.invT - m1) * kLog2e) * inv_s1;
+                    w.z = ex2((a.z * p.invT - m1) * kLog2e) * inv_s1;
+                    w.w = ex2((a.w * p.invT - m1) * kLog2e) * inv_s1;
+                }
+                w4[k] = w;
+                acc += (w.x + w.y) + (w.z + w.w);
+            }
+        } else {
 #pragma unroll 4
-    for (int k = t; k < n; k += kST) {
-        const float x = sz[k] * p.invT;
-        const float pk = ex2((x - m1) * kLog2e) * inv_s1;
-        float w = pk;
-        if (resid) {
-            const float qk = sq[k];
-            const float a = fmaf(p.eta, qk - pk, x);
-            float ph = ex2((a - m2) * kLog2e) * inv_s2;
-            if (ph < thr) ph = pk;
-            w = fmaxf(fmaxf(pk - ph, pk - qk), 0.f);
+            for (int k = t; k < n; k += kST) {
+                const float w = resid ? resid_weight(zr[k], qr[k], p.invT, p.eta, m1, inv_s1, m2,
+                                                     inv_s2, thr)
+                                      : ex2((zr[k] * p.invT - m1) * kLog2e) * inv_s1;
+                sw[k] = w;
+                acc += w;
+            }
         }
-        sz[k] = w;
+        acc = warp_sum(acc);
+        if (lane == 0) s_seg[warp] = acc;
+        __syncthreads();
+        if (t == 0) {
+            float tot = 0.f;
+            for (int w = 0; w < kSW; ++w) tot += s_seg[w];
+            s_total[0] = tot;
+        }
+        cluster.sync();   // every slice's total is in place
+        if (warp == 0) {   // the cluster's totals, in slice order
+            const float mc = lane < p.C ? *cluster.map_shared_rank(&s_total[0], lane) : 0.f;
+            const float totals = warp_sum(mc);
+            const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
+            const float target = word_uniform(rnd.w[1]) * totals;
+            float incl = mc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, mc > 0.f && incl > target);
+            const unsigned pos = __ballot_sync(0xffffffffu, mc > 0.f);
+            int owner = -1;
+            float tin = INFINITY;
+            if (hit) {
+                owner = __ffs(hit) - 1;
+                tin = target - __shfl_sync(0xffffffffu, incl - mc, owner);
+            } else if (pos) {
+                owner = 31 - __clz(pos);   // rounding left the target past the end
+            }
+            if (lane == 0) {
+                s_owner = owner;
+                s_tin = tin;
+                s_total[1] = totals;
+            }
+        }
+        cluster.sync();   // every CTA has read the totals: they may be rewritten, the CTAs may leave
+        if (!resid || s_total[1] > 0.f) break;
+        resid = false;
     }
-    __syncthreads();
+    const int owner = s_owner;
+    if (owner < 0) {   // no mass at all (degenerate input)
+        if (cs == 0 && t == 0) p.next_token[b] = 0;
+        return;
+    }
+    if (cs != owner) return;
+    const float tin = s_tin;
     // one contiguous segment per warp: its sum, then the warp whose segment holds the target
     const int seg = (n + kSW * 32 - 1) / (kSW * 32) * 32;
     const int g0 = warp * seg;
     const int g1 = min(n, g0 + seg);
     float acc = 0.f;
-    for (int k = g0 + lane; k < g1; k += 32) acc += sz[k];
+    for (int k = g0 + lane; k < g1; k += 32) acc += sw[k];
     acc = warp_sum(acc);
     if (lane == 0) s_seg[warp] = acc;
     __syncthreads();
@@ -806,7 +769,7 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
     }
     __syncthreads();
     const int ow = s_ow;
-    if (ow < 0) {   // the recomputed slice has no mass: first entry of the slice
+    if (ow < 0) {   // the owner slice has no mass (rounding): its first entry
         if (t == 0) p.next_token[b] = (int)lo;
         return;
     }
@@ -818,7 +781,7 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
         const int a0 = min(g1, g0 + lane * per);
         const int a1 = min(g1, a0 + per);
         float ls = 0.f;
-        for (int k = a0; k < a1; ++k) ls += sz[k];
+        for (int k = a0; k < a1; ++k) ls += sw[k];
         float incl = ls;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -839,7 +802,7 @@ __global__ void __launch_bounds__(kST) accept_select_kernel(const AcceptParams p
             float ce = 0.f;
             int kpick = -1, klast = -1;
             for (int k = a0; k < a1; ++k) {
-                const float w = sz[k];
+                const float w = sw[k];
                 if (w > 0.f) {
                     klast = k;
                     if (ce + w > tl) {
@@ -1011,20 +974,28 @@ cudaError_t launch_accept(const AcceptParams& p0, const AcceptShape& sh, cudaStr
     if (p.nclusters < 1) return cudaErrorNotSupported;
     cudaError_t e = launch_rows_dispatch(sh.F, p, st);
     if (e != cudaSuccess) return e;
-    const size_t sel_smem = (size_t)p.chunk * 8;
+    const size_t sel_smem = (size_t)p.chunk * 4;
     e = cudaFuncSetAttribute(accept_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sel_smem);
     if (e != cudaSuccess) return e;
+    if (p.C > 8) {
+        e = cudaFuncSetAttribute(accept_select_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.B, 1, 1);
+    cfg.gridDim = dim3(p.C, p.B, 1);
     cfg.blockDim = dim3(kST, 1, 1);
     cfg.dynamicSmemBytes = sel_smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = p.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, accept_select_kernel, p);
 }
 

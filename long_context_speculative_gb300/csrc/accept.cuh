@@ -20,7 +20,6 @@ struct AcceptParams {
     const int32_t* parent;       // [B, n_q] or nullptr (chain)
     int32_t* ws_accept;          // [B * n_q] ratio-test outcome of node i
     float* ws_stats;             // [B * n_q, 4] (m1, s1), (m2, s2) of row j: softmax = exp(. - m) / s
-    float* ws_mass;              // [B * n_q, kAcceptMaxCluster, 2] residual mass, p mass per slice
     float* diag;                 // [B, n_q, 5] or nullptr
     int32_t* n_accepted;         // [B]
     int32_t* next_token;         // [B]

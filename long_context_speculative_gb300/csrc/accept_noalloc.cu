@@ -6,8 +6,8 @@
 // plug-ins no allocator, or a latency-critical decode loop that must never
 // call cudaMalloc (which may synchronise the device).  For them this entry
 // point takes only inputs and outputs.  Its scratch (per node: the ratio-test
-// outcome, the row's softmax statistics, and the residual and p mass of each
-// of up to 16 vocabulary slices; 592 KB for 4096 nodes) lives in the array
+// outcome and the row's softmax statistics, 20 bytes; 80 KB for 4096 nodes)
+// lives in the array
 // below, which every GPU that loads librapid.so holds until the process
 // exits.  The verification step of the pages has no counterpart of this; it
 // is a packaging variant of rapid_accept.
@@ -21,11 +21,10 @@ namespace rapid {
 namespace {
 
 constexpr size_t align256(size_t n) { return (n + 255) / 256 * 256; }
-// The layout rapid_accept_workspace_size describes, at its largest cluster (16).
+// The layout rapid_accept_workspace_size describes.
 constexpr size_t kNodes = (size_t)RAPID_NOALLOC_MAX_NODES;
 constexpr size_t kScratchBytes = align256(kNodes * sizeof(int32_t)) +
-                                 align256(kNodes * 4 * sizeof(float)) +
-                                 align256(kNodes * 16 * 2 * sizeof(float));
+                                 align256(kNodes * 4 * sizeof(float));
 
 // Shared by every call on a device; see the concurrency note in rapid.h.
 static __device__ __align__(256) unsigned char g_accept_scratch[kScratchBytes];

@@ -163,9 +163,7 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
 size_t rapid_accept_workspace_size(int B, int n_q, int V) {
     if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return 0;
     const size_t rows = (size_t)B * n_q;
-    const size_t C = (size_t)kAcceptMaxCluster;
-    return align_up(rows * sizeof(int32_t)) + align_up(rows * 4 * sizeof(float)) +
-           align_up(rows * C * 2 * sizeof(float));
+    return align_up(rows * sizeof(int32_t)) + align_up(rows * 4 * sizeof(float));
 }
 
 rapid_status rapid_accept(const float* z_target, const float* q_draft, const int32_t* draft_tokens,
@@ -197,8 +195,6 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft, const int
     p.ws_accept = reinterpret_cast<int32_t*>(ws);
     ws += align_up(rows * sizeof(int32_t));
     p.ws_stats = reinterpret_cast<float*>(ws);
-    ws += align_up(rows * 4 * sizeof(float));
-    p.ws_mass = reinterpret_cast<float*>(ws);
     p.diag = diag; p.n_accepted = n_accepted; p.next_token = next_token; p.path = path;
     p.B = B; p.n_q = n_q; p.V = V;
     p.bulk = ((V % 4) == 0 && aligned16(z_target) && aligned16(q_draft)) ? 1 : 0;
