@@ -82,6 +82,17 @@ def test_group_widths(G, n_q):
     _run_and_check(w)
 
 
+@pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False)])
+def test_pair_widths_ragged(G, n_q, tree):
+    # 129..256 group rows run on CTA pairs (each CTA loads half of every K/V
+    # tile); ragged prefixes include an empty history and a single key
+    w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=128, n_q=n_q, prefix=2100, layers=1, V=10,
+                    dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, tree=tree,
+                    tree_nodes_max_depth=6, seed=60 + G + n_q)
+    _run_and_check(w, prefix_override=[0, 1, 2100])
+    _run_and_check(w, prefix_override=[63, 1000, 65])
+
+
 def test_custom_scale_and_fp32_d128():
     w = wl.Workload("t", B=2, Hq=6, Hkv=3, d=128, n_q=4, prefix=700, prefix_lo=650, layers=1,
                     V=10, dtype="f32", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=51)
