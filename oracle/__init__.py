@@ -15,6 +15,8 @@ the passages it follows:
 * acceptance: "RAPID: Long-Context Inference with Retrieval-Augmented
   Speculative Decoding" (blog summary), sections 2.1 and 2.4.
 * random numbers: Philox4x32-10 (Salmon et al., SC'11).
+* KV commit after acceptance: the accepted path's speculative rows join the
+  history after the root, in path order (``kv_commit``, ``kv_advance``).
 """
 import ctypes
 import os
@@ -66,6 +68,10 @@ def lib():
         L.orc_accept.argtypes = [_fp, _fp, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_double, ctypes.c_double, ctypes.c_uint64, ctypes.c_int,
                                  _i32p, _i32p, _i32p, _dp, _dp, ctypes.c_int]
+        L.orc_kv_commit.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p]
+        L.orc_kv_commit.restype = ctypes.c_int
+        L.orc_kv_advance.argtypes = [_i32p, _i32p, ctypes.c_int]
         L.orc_first_token_hist.argtypes = [_fp, _fp, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, ctypes.c_int, ctypes.c_uint64,
                                            ctypes.c_int64, _i64p, ctypes.c_int]
@@ -259,3 +265,28 @@ def first_token_hist(z, q, T, eta, clamp, seed, n_trials, nthreads=None):
                                int(bool(clamp)), int(seed), int(n_trials), _ptr(hist, _i64p),
                                nthreads or default_threads())
     return hist
+
+
+def kv_commit(K, V, prefix_len, path, n_accepted):
+    """In place on numpy caches K, V [layers, B, Hkv, cap, d] (any dtype): row
+    P_b + 1 + k of every (layer, b, head) takes the row of node path[b][k].
+    Returns the number of sequences left untouched (invalid input)."""
+    assert K.shape == V.shape and K.flags.c_contiguous and V.flags.c_contiguous
+    layers, B, Hkv, cap = K.shape[:4]
+    row_bytes = int(np.prod(K.shape[4:])) * K.itemsize
+    n_q = path.shape[1]
+    kb = K.view(np.uint8).reshape(-1)
+    vb = V.view(np.uint8).reshape(-1)
+    pl = _c(prefix_len, np.int32)
+    pa = _c(path, np.int32)
+    na = _c(n_accepted, np.int32)
+    return int(lib().orc_kv_commit(_ptr(kb, _u8p), _ptr(vb, _u8p), layers, B, Hkv, cap, row_bytes,
+                                   n_q, _ptr(pl, _i32p), _ptr(pa, _i32p), _ptr(na, _i32p)))
+
+
+def kv_advance(prefix_len, n_accepted):
+    """New history lengths: P_b + 1 + n_accepted[b]."""
+    pl = _c(prefix_len, np.int32).copy()
+    na = _c(n_accepted, np.int32)
+    lib().orc_kv_advance(_ptr(pl, _i32p), _ptr(na, _i32p), pl.shape[0])
+    return pl

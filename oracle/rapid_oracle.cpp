@@ -36,6 +36,14 @@
  *
  * Parity of the tree path-selection rule is unpinned beyond brute-force
  * enumeration of tiny trees (the pages define only the tree mask).
+ *
+ * KV commit (the step after acceptance; the pages describe the verify pass's
+ * cache layout -- [LongSpec] section 2.3, speculative rows after the history,
+ * node i of the step at position P + i, node 0 the root -- but print no
+ * commit step): the accepted path's rows, already computed by the verify
+ * pass, join the history right after the root in path order, and the history
+ * length grows by 1 + n_accepted; the other speculative rows are dropped by
+ * not counting them.
  */
 #include <algorithm>
 #include <cmath>
@@ -423,6 +431,51 @@ void accept_one(const AcceptProblem& A, int b, int32_t* n_acc, int32_t* next_tok
 extern "C" {
 
 int orc_version(void) { return 1; }
+
+// K, V: [layers, B, Hkv, cap, row_bytes] opaque rows.  For every (layer, b, h)
+// and k < n_acc[b]: row P_b + 1 + k takes the row that node path[b][k] had
+// (P_b = prefix_len[b]), all sources read before any destination is written.
+// A sequence with an invalid input (n_acc outside [0, n_q - 1], P_b < 0,
+// P_b + n_q > cap, a path entry outside [k + 1, n_q - 1] or not increasing) is
+// left untouched; returns how many sequences were.
+int orc_kv_commit(uint8_t* K, uint8_t* V, int layers, int B, int Hkv, int64_t cap, int row_bytes,
+                  int n_q, const int32_t* prefix_len, const int32_t* path, const int32_t* n_acc) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_acc[b];
+        const int64_t P = prefix_len[b];
+        bool ok = n >= 0 && n <= n_q - 1 && P >= 0 && P + n_q <= cap;
+        for (int k = 0; ok && k < n; ++k) {
+            const int src = path[(int64_t)b * n_q + k];
+            if (src < k + 1 || src > n_q - 1) ok = false;
+            if (k > 0 && src <= path[(int64_t)b * n_q + k - 1]) ok = false;
+        }
+        if (!ok) {
+            ++bad;
+            continue;
+        }
+        std::vector<uint8_t> rows((size_t)n * row_bytes);
+        for (int l = 0; l < layers; ++l) {
+            for (int h = 0; h < Hkv; ++h) {
+                for (uint8_t* cache : {K, V}) {
+                    uint8_t* base = cache + ((((int64_t)l * B + b) * Hkv + h) * cap + P) * row_bytes;
+                    for (int k = 0; k < n; ++k)
+                        std::memcpy(&rows[(size_t)k * row_bytes],
+                                    base + (int64_t)path[(int64_t)b * n_q + k] * row_bytes, row_bytes);
+                    for (int k = 0; k < n; ++k)
+                        std::memcpy(base + (int64_t)(1 + k) * row_bytes, &rows[(size_t)k * row_bytes],
+                                    row_bytes);
+                }
+            }
+        }
+    }
+    return bad;
+}
+
+// The history after a committed step: the root and the accepted rows join it.
+void orc_kv_advance(int32_t* prefix_len, const int32_t* n_acc, int B) {
+    for (int b = 0; b < B; ++b) prefix_len[b] += 1 + n_acc[b];
+}
 
 void orc_philox4x32_10(const uint32_t* ctr, const uint32_t* key, uint32_t* out) {
     philox4x32_10(ctr, key, out);
