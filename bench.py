@@ -236,9 +236,12 @@ def run_gpu(args, w):
     acc_in = wl.accept_inputs(w, parents=parents if w.tree else None)
     z = acc_in.z.to(dev); q = acc_in.q.to(dev); tok = acc_in.tokens.to(dev)
     par = None if acc_in.parent is None else acc_in.parent.to(dev)
-    Os = [torch.empty_like(Qs[0]) for _ in range(w.layers)]
-    Ls = [torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
-          for _ in range(w.layers)]
+    # every layer's O and LSE in one tensor each, so that the end-to-end leg
+    # reads them back with one copy apiece
+    O_all = torch.empty((w.layers,) + tuple(Qs[0].shape), dtype=Qs[0].dtype, device=dev)
+    L_all = torch.empty((w.layers, w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
+    Os = list(O_all.unbind(0))
+    Ls = list(L_all.unbind(0))
     ws_attn = torch.empty(rapid.rapid_verify_attn_workspace_size(
         w.B, w.Hq, w.Hkv, w.d, w.n_q, cap, rapid.RAPID_DTYPE_BF16), dtype=torch.uint8, device=dev)
     ws_acc = torch.empty(rapid.rapid_accept_workspace_size(w.B, w.n_q, w.V), dtype=torch.uint8,
@@ -311,9 +314,8 @@ def run_gpu(args, w):
                                     Os[layer], Ls[layer], ws_attn)
         rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
                            res_dev[:w.B], res_dev[w.B:], None, None, ws_acc)
-        for layer in range(w.layers):
-            hO[layer].copy_(Os[layer], non_blocking=True)
-            hL[layer].copy_(Ls[layer], non_blocking=True)
+        hO.copy_(O_all, non_blocking=True)
+        hL.copy_(L_all, non_blocking=True)
         hres.copy_(res_dev, non_blocking=True)
 
     for i in range(args.warmup):
@@ -334,6 +336,9 @@ def run_gpu(args, w):
 
     # ---- acceptance bandwidth on a batch larger than L2 -----------------------
     acc_roof = accept_batch_roofline(w, dev, stream)
+
+    # ---- KV commit of an accepted path, all layers (moves the cache rows last) -
+    kv_commit = kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream)
 
     # ---- numbers -----------------------------------------------------------
     ms_per_step = total_ms / args.steps
@@ -366,6 +371,7 @@ def run_gpu(args, w):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "accept_roofline": acc_roof,
+            "kv_commit": kv_commit,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": wall}
@@ -378,6 +384,36 @@ def run_gpu(args, w):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
+    """rapid_kv_commit over every layer for an accepted path that moves rows
+    (nodes 2, 4, 6, ...: every destination differs from its source).  The
+    moved bytes are tiny, so this is a latency figure, not a bandwidth one."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+
+    n = (w.n_q - 1) // 2
+    path = torch.full((w.B, w.n_q), -1, dtype=torch.int32)
+    path[:, :n] = torch.arange(2, 2 * n + 1, 2, dtype=torch.int32)
+    path = path.to(dev)
+    n_acc = torch.full((w.B,), n, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        rapid.rapid_kv_commit(Ks, Vs, prefix_len, path, n_acc)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        rapid.rapid_kv_commit(Ks, Vs, prefix_len, path, n_acc)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert rapid.rapid_device_error(True) == 0
+    moved = w.layers * w.B * w.Hkv * n * w.d * 2 * 2   # K and V rows, bf16
+    return {"us_per_step": e0.elapsed_time(e1) / reps * 1e3, "layers": w.layers,
+            "rows_moved_per_layer": w.B * w.Hkv * n, "bytes_moved": moved,
+            "launches_per_step": 1}
 
 
 def accept_batch_roofline(w, dev, stream, reps=20):

@@ -233,7 +233,8 @@ int rapid_version(void);
 /*
  * Sticky error bits that kernels of this library raised on the CURRENT device
  * (bit 0: a bounded wait for an asynchronous copy gave up, so the outputs of
- * that call are invalid).  Synchronises the device to read the word; clears it
+ * that call are invalid; bit 1: rapid_kv_commit or rapid_kv_advance found an
+ * invalid device-side input and left that sequence alone).  Synchronises the device to read the word; clears it
  * when `clear` is non-zero.  Returns -1 if the word could not be read.
  */
 int rapid_device_error(int clear);
@@ -246,6 +247,63 @@ int rapid_device_error(int clear);
  * Returns 0 on success, -1 if the record could not be read.
  */
 int rapid_device_error_info(uint32_t* words8, int clear);
+
+/* ------------------------------------------------------------------------ */
+/* KV commit after acceptance                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Most layers one rapid_kv_commit call takes. */
+enum { RAPID_COMMIT_MAX_LAYERS = 128 };
+
+/*
+ * Keep the accepted speculative K/V rows of a verify step and drop the rest.
+ * In the verify pass the n_q tokens of a step sit after the history of every
+ * layer's cache, node i at row P_b + i with node 0 the root ("LongSpec:
+ * Long-Context Lossless Speculative Decoding with Efficient Drafting and
+ * Verification", section 2.3, the hybrid tree attention layout).  After
+ * acceptance the accepted path's rows, already computed by the verify pass,
+ * join the history right after the root, in path order:
+ *
+ *   K[b, h, P_b + 1 + k, :] := K[b, h, P_b + path[b][k], :]   for k < n_accepted[b]
+ *
+ * and the same for V, for every KV head h of every layer.  Rows past
+ * P_b + n_accepted[b] are left as they are (the next step overwrites them).
+ * A chain's path is 1, 2, ..., so nothing moves.  Call rapid_kv_advance after
+ * the last layer to grow the history lengths.
+ *
+ *  K_layers, V_layers  HOST arrays of `layers` device pointers; layer l's
+ *                      caches are [B, Hkv, kv_capacity, d] of dtype
+ *                      (RAPID_DTYPE_F32 or RAPID_DTYPE_BF16), 16-byte aligned.
+ *  prefix_len          device int32 [B]: P_b, the history length before the
+ *                      step (the root's row).
+ *  path, n_accepted    device int32 [B, n_q] and [B], as rapid_accept writes
+ *                      them: the accepted node ids in root-to-leaf order.
+ *
+ * Sources are read before destinations are written, so overlapping moves
+ * (path 2, 3, ...) are safe.  Errors: RAPID_EINVAL for NULL pointers, layers
+ * outside [1, RAPID_COMMIT_MAX_LAYERS], B < 1, Hkv < 1, d not 64 or 128, n_q
+ * outside [1, RAPID_MAX_NQ], kv_capacity < 1, a bad dtype or unaligned caches;
+ * RAPID_ECUDA when the launch fails.  A sequence whose device inputs are
+ * invalid (n_accepted outside [0, n_q - 1], P_b + n_q > kv_capacity, a path
+ * entry outside [k + 1, n_q - 1] or not increasing) is left untouched and bit
+ * 1 of the device error word is set.
+ */
+rapid_status rapid_kv_commit(void* const* K_layers, void* const* V_layers, int layers, int dtype,
+                             int B, int Hkv, int d, int64_t kv_capacity, int n_q,
+                             const int32_t* prefix_len, const int32_t* path,
+                             const int32_t* n_accepted, void* stream);
+
+/*
+ * prefix_len[b] += 1 + n_accepted[b] on the device (the root and the accepted
+ * drafts join the history).  A sequence whose n_accepted is outside
+ * [0, n_q - 1] or whose P_b + n_q exceeds kv_capacity keeps its length and
+ * sets bit 1 of the device error word.  Errors: RAPID_EINVAL for NULL
+ * pointers, B < 1, n_q outside [1, RAPID_MAX_NQ], kv_capacity < 1;
+ * RAPID_ECUDA on launch failure.
+ */
+rapid_status rapid_kv_advance(int32_t* prefix_len, const int32_t* n_accepted, int B, int n_q,
+                              int64_t kv_capacity, void* stream);
+
 
 #ifdef __cplusplus
 }

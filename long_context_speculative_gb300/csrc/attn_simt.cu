@@ -190,6 +190,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnParams p) {
     constexpr int VPL = D / 32;                 // columns per lane
     __shared__ float s_w[kMergeMaxS];           // partial weights 2^(m_s - M)
+    __shared__ float2 s_ml[kMergeMaxS];         // (m_s, l_s) of the partials
     __shared__ float s_red[4][D];
     __shared__ float s_scal[4][2];
     __shared__ float s_spec[2];                 // m_spec, l_spec (relative to m_spec)
@@ -245,10 +246,23 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
         }
         if (lane == 0) { s_spec[0] = m_spec; s_spec[1] = l_spec; }
     }
+    // ---- the first partial rows into registers at once (warp w takes the
+    // partials w, w + 4, ...), while the (m, l) pairs are reduced: one round of
+    // memory latency instead of three
+    constexpr int kPre = 8;                      // partial rows per warp held in registers
+    float v[kPre][VPL];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+        const int sp = warp + 4 * u;
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) v[u][c] = sp < nparts ? pa[sp * pas + lane * VPL + c] : 0.f;
+    }
     // ---- M over the history partials -------------------------------------
     float mloc = -INFINITY;
     for (int s = tid; s < nparts; s += kMergeThreads) {
-        if (ml[s * mls + 1] > 0.f) mloc = fmaxf(mloc, ml[s * mls]);
+        const float2 x = *reinterpret_cast<const float2*>(ml + s * mls);
+        s_ml[s] = x;
+        if (x.y > 0.f) mloc = fmaxf(mloc, x.x);
     }
     mloc = warp_max(mloc);
     if (lane == 0) s_scal[warp][0] = mloc;
@@ -258,10 +272,10 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     // ---- weights and L ---------------------------------------------------
     float lloc = 0.f;
     for (int s = tid; s < nparts; s += kMergeThreads) {
-        const float ls = ml[s * mls + 1];
-        const float w = ls > 0.f ? exp2f(ml[s * mls] - M) : 0.f;
+        const float2 x = s_ml[s];
+        const float w = x.y > 0.f ? exp2f(x.x - M) : 0.f;
         s_w[s] = w;
-        lloc = fmaf(w, ls, lloc);
+        lloc = fmaf(w, x.y, lloc);
     }
     lloc = warp_sum(lloc);
     if (lane == 0) s_scal[warp][1] = lloc;
@@ -272,21 +286,14 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     float acc[VPL];
 #pragma unroll
     for (int c = 0; c < VPL; ++c) acc[c] = 0.f;
-    int s = warp;
-    for (; s + 12 < nparts; s += 16) {
-        float v[4][VPL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kPre; ++u) {
+        const int sp = warp + 4 * u;
+        const float w = sp < nparts ? s_w[sp] : 0.f;
 #pragma unroll
-            for (int c = 0; c < VPL; ++c) v[u][c] = pa[(s + 4 * u) * pas + lane * VPL + c];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float w = s_w[s + 4 * u];
-#pragma unroll
-            for (int c = 0; c < VPL; ++c) acc[c] = fmaf(w, w != 0.f ? v[u][c] : 0.f, acc[c]);
-        }
+        for (int c = 0; c < VPL; ++c) acc[c] = fmaf(w, w != 0.f ? v[u][c] : 0.f, acc[c]);
     }
-    for (; s < nparts; s += 4) {
+    for (int s = warp + 4 * kPre; s < nparts; s += 4) {
         const float w = s_w[s];
         if (w == 0.f) continue;
 #pragma unroll

@@ -6,6 +6,7 @@
 #include "accept.cuh"
 #include "attn.cuh"
 #include "common.cuh"
+#include "kv_commit.cuh"
 #include "rapid.h"
 
 namespace rapid {
@@ -220,6 +221,47 @@ const char* rapid_status_string(int status) {
 }
 
 int rapid_version(void) { return 100; }
+
+rapid_status rapid_kv_commit(void* const* K_layers, void* const* V_layers, int layers, int dtype,
+                             int B, int Hkv, int d, int64_t kv_capacity, int n_q,
+                             const int32_t* prefix_len, const int32_t* path,
+                             const int32_t* n_accepted, void* stream) {
+    if (!K_layers || !V_layers || !prefix_len || !path || !n_accepted) return RAPID_EINVAL;
+    if (layers < 1 || layers > RAPID_COMMIT_MAX_LAYERS || B < 1 || Hkv < 1) return RAPID_EINVAL;
+    if ((d != 64 && d != 128) || n_q < 1 || n_q > RAPID_MAX_NQ || kv_capacity < 1) return RAPID_EINVAL;
+    if (dtype != RAPID_DTYPE_F32 && dtype != RAPID_DTYPE_BF16) return RAPID_EINVAL;
+    CommitParams p{};
+    for (int l = 0; l < layers; ++l) {
+        if (!K_layers[l] || !V_layers[l] || !aligned16(K_layers[l]) || !aligned16(V_layers[l]))
+            return RAPID_EINVAL;
+        p.K[l] = K_layers[l];
+        p.V[l] = V_layers[l];
+    }
+    if (n_q == 1) return RAPID_OK;   // no draft node: nothing can move
+    p.prefix_len = prefix_len;
+    p.path = path;
+    p.n_acc = n_accepted;
+    p.err = device_error_word();
+    p.cap = kv_capacity;
+    p.layers = layers;
+    p.B = B;
+    p.Hkv = Hkv;
+    p.n_q = n_q;
+    p.row_bytes = d * (dtype == RAPID_DTYPE_BF16 ? 2 : 4);
+    return launch_kv_commit(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RAPID_OK
+                                                                                 : RAPID_ECUDA;
+}
+
+rapid_status rapid_kv_advance(int32_t* prefix_len, const int32_t* n_accepted, int B, int n_q,
+                              int64_t kv_capacity, void* stream) {
+    if (!prefix_len || !n_accepted || B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || kv_capacity < 1)
+        return RAPID_EINVAL;
+    return launch_kv_advance(prefix_len, n_accepted, B, n_q, kv_capacity, device_error_word(),
+                             static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RAPID_OK
+               : RAPID_ECUDA;
+}
+
 
 int rapid_device_error(int clear) {
     uint32_t w[8];

@@ -12,7 +12,7 @@ namespace rapid {
 // Bits of the sticky per-device error word (defined in capi.cu; kernels get
 // its address as a parameter and only ever OR bits into it; the host reads
 // and clears it through rapid_device_error()).
-enum : unsigned int { kErrWaitTimeout = 1u };
+enum : unsigned int { kErrWaitTimeout = 1u, kErrBadInput = 2u };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;

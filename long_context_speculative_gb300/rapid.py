@@ -21,6 +21,7 @@ RAPID_DTYPE_BF16 = 1
 RAPID_ACCEPT_TAIL_CLAMP = 1
 RAPID_MAX_NQ = 64
 RAPID_MAX_VOCAB = 229376
+RAPID_COMMIT_MAX_LAYERS = 128
 
 _lib = None
 
@@ -62,6 +63,10 @@ def lib() -> ctypes.CDLL:
     L.rapid_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp,
                                        vp, vp, vp]
     L.rapid_accept_noalloc.restype = i32
+    L.rapid_kv_commit.argtypes = [vp, vp, i32, i32, i32, i32, i32, i64, i32, vp, vp, vp, vp]
+    L.rapid_kv_commit.restype = i32
+    L.rapid_kv_advance.argtypes = [vp, vp, i32, i32, i64, vp]
+    L.rapid_kv_advance.restype = i32
     _lib = L
     return L
 
@@ -146,6 +151,33 @@ def rapid_accept_noalloc(z_target, q_draft, draft_tokens, parent, T, eta, philox
                                     _ptr(n_accepted), _ptr(next_token), _ptr(path), _ptr(diag),
                                     _stream(stream))
     _check(st, "rapid_accept_noalloc")
+
+
+def rapid_kv_commit(K_layers, V_layers, prefix_len, path, n_accepted, stream=None):
+    """Move the accepted speculative K/V rows of every layer next to the root.
+
+    K_layers, V_layers: sequences of [B, Hkv, kv_capacity, d] caches (one per
+    layer); prefix_len [B], path [B, n_q], n_accepted [B] int32 on the device."""
+    if len(K_layers) != len(V_layers) or not K_layers:
+        raise RapidError("rapid_kv_commit needs matching, non-empty K and V layer lists")
+    _need_cuda(*K_layers, *V_layers, prefix_len, path, n_accepted)
+    B, Hkv, cap, d = K_layers[0].shape
+    n_q = path.shape[1]
+    layers = len(K_layers)
+    karr = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in K_layers])
+    varr = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in V_layers])
+    st = lib().rapid_kv_commit(ctypes.cast(karr, ctypes.c_void_p), ctypes.cast(varr, ctypes.c_void_p),
+                               layers, _dtype_code(K_layers[0]), B, Hkv, d, cap, n_q,
+                               _ptr(prefix_len), _ptr(path), _ptr(n_accepted), _stream(stream))
+    _check(st, "rapid_kv_commit")
+
+
+def rapid_kv_advance(prefix_len, n_accepted, n_q, kv_capacity, stream=None):
+    """prefix_len += 1 + n_accepted (device, in place)."""
+    _need_cuda(prefix_len, n_accepted)
+    st = lib().rapid_kv_advance(_ptr(prefix_len), _ptr(n_accepted), prefix_len.shape[0], n_q,
+                                kv_capacity, _stream(stream))
+    _check(st, "rapid_kv_advance")
 
 
 def rapid_device_error(clear: bool = True) -> int:

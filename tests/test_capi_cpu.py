@@ -58,6 +58,27 @@ def test_host_validation_without_gpu(lib):
     assert lib.rapid_verify_attn_workspace_size(1, 32, 8, 128, 11, 122896, 1) > 0
 
 
+def test_kv_commit_host_validation_without_gpu(lib):
+    arr = (ctypes.c_void_p * 1)(16)   # a fake, aligned device address (never dereferenced)
+    good = [ctypes.cast(arr, ctypes.c_void_p), ctypes.cast(arr, ctypes.c_void_p), 1, 1, 2, 2, 128,
+            4096, 8, ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), None]
+    for i, bad in [(0, None), (2, 0), (2, 129), (3, 5), (4, 0), (5, 0), (6, 96), (7, 0), (8, 0),
+                   (8, 65), (9, None), (10, None), (11, None)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.rapid_kv_commit(*args) == -1, i
+    unaligned = (ctypes.c_void_p * 1)(8)
+    args = list(good)
+    args[0] = ctypes.cast(unaligned, ctypes.c_void_p)
+    assert lib.rapid_kv_commit(*args) == -1
+    args = list(good)
+    args[8] = 1   # n_q = 1: no draft node, nothing to launch
+    assert lib.rapid_kv_commit(*args) == 0
+    assert lib.rapid_kv_advance(None, ctypes.c_void_p(16), 1, 8, 4096, None) == -1
+    assert lib.rapid_kv_advance(ctypes.c_void_p(16), ctypes.c_void_p(16), 0, 8, 4096, None) == -1
+    assert lib.rapid_kv_advance(ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 65, 4096, None) == -1
+
+
 def test_no_cpu_fallback_for_cpu_tensors(lib):
     import torch
     Q = torch.zeros((1, 4, 5, 128), dtype=torch.bfloat16)
