@@ -396,7 +396,8 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
 
     n = (w.n_q - 1) // 2
     path = torch.full((w.B, w.n_q), -1, dtype=torch.int32)
-    path[:, :n] = torch.arange(2, 2 * n + 1, 2, dtype=torch.int32)
+    if n > 0:
+        path[:, :n] = torch.arange(2, 2 * n + 1, 2, dtype=torch.int32)
     path = path.to(dev)
     n_acc = torch.full((w.B,), n, dtype=torch.int32, device=dev)
     for _ in range(3):
@@ -425,7 +426,9 @@ def accept_batch_roofline(w, dev, stream, reps=20):
     from long_context_speculative_gb300 import rapid
     from long_context_speculative_gb300 import workloads as wl
 
-    Bb = 16   # 16 independent sequences of the workload's rows: > 100 MB, > L2
+    # 16 independent sequences of the workload's rows, more if that stays under
+    # 100 MB (so that the batch is larger than L2)
+    Bb = max(16, -(-100_000_000 // (w.n_q * w.V * 8)))
     inp = wl.accept_inputs(w, B=Bb, parents=None if not w.tree else None)
     z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
     par = None if inp.parent is None else inp.parent.to(dev)

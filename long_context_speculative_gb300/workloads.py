@@ -80,8 +80,15 @@ QWEN7B_TREE_1LAYER = Workload("qwen2.5-7b_tree32_1layer", B=4, Hq=28, Hkv=4, d=1
                               z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
                               tree=True, seed=1005)
 
+# single-query decode attention over the same 120K cache (one query row per
+# query head: the draft-side / plain decode shape of the split-KV pass)
+LLAMA8B_DECODE_120K = Workload("llama3.1-8b_decode_32layers_120k", B=1, Hq=32, Hkv=8, d=128,
+                               n_q=1, prefix=122880, layers=32, V=128256, dtype="bf16",
+                               z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
+                               seed=1007)
+
 ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA8B_1LAYER_120K, LLAMA70B_128K, QWEN7B_TREE,
-       QWEN7B_TREE_1LAYER]
+       QWEN7B_TREE_1LAYER, LLAMA8B_DECODE_120K]
 
 
 def gen(seed: int, device="cpu") -> torch.Generator:

@@ -75,7 +75,7 @@ def test_prefix_fills_capacity():
     _run_and_check(w, capacity=1024)
 
 
-@pytest.mark.parametrize("G,n_q", [(1, 1), (1, 64), (8, 11), (7, 32), (16, 5)])
+@pytest.mark.parametrize("G,n_q", [(1, 1), (4, 1), (1, 64), (8, 11), (7, 32), (16, 5)])
 def test_group_widths(G, n_q):
     w = wl.Workload("t", B=1, Hq=2 * G, Hkv=2, d=128, n_q=n_q, prefix=900, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=40 + G)
@@ -91,6 +91,13 @@ def test_pair_widths_ragged(G, n_q, tree):
                     tree_nodes_max_depth=6, seed=60 + G + n_q)
     _run_and_check(w, prefix_override=[0, 1, 2100])
     _run_and_check(w, prefix_override=[63, 1000, 65])
+
+
+def test_decode_single_query_ragged():
+    # one query row per head (decode / draft-side shape), ragged long histories
+    w = wl.Workload("t", B=3, Hq=32, Hkv=8, d=128, n_q=1, prefix=9000, layers=1, V=10,
+                    dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=71)
+    _run_and_check(w, prefix_override=[9000, 17, 0])
 
 
 def test_custom_scale_and_fp32_d128():
