@@ -17,6 +17,8 @@ the passages it follows:
 * random numbers: Philox4x32-10 (Salmon et al., SC'11).
 * KV commit after acceptance: the accepted path's speculative rows join the
   history after the root, in path order (``kv_commit``, ``kv_advance``).
+* retrieval for the draft's compressed context: "RAPID ..." section 3.1, RAG
+  settings (``retrieval_scores``, ``retrieval_select``).
 """
 import ctypes
 import os
@@ -72,6 +74,10 @@ def lib():
                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int, _i32p, _i32p, _i32p]
         L.orc_kv_commit.restype = ctypes.c_int
         L.orc_kv_advance.argtypes = [_i32p, _i32p, ctypes.c_int]
+        L.orc_retrieval_scores.argtypes = [_fp, _fp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp]
+        L.orc_retrieval_select.argtypes = [_fp, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_float, ctypes.c_int, ctypes.c_int, _i32p,
+                                           _i32p, _i32p]
         L.orc_first_token_hist.argtypes = [_fp, _fp, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, ctypes.c_int, ctypes.c_uint64,
                                            ctypes.c_int64, _i64p, ctypes.c_int]
@@ -290,3 +296,27 @@ def kv_advance(prefix_len, n_accepted):
     na = _c(n_accepted, np.int32)
     lib().orc_kv_advance(_ptr(pl, _i32p), _ptr(na, _i32p), pl.shape[0])
     return pl
+
+
+def retrieval_scores(query, chunks):
+    """Cosine similarities [B, N] (double) of chunks [B, N, D] with query [B, D] (float32)."""
+    q = _c(query, np.float32)
+    c = _c(chunks, np.float32)
+    B, N, D = c.shape
+    out = np.zeros((B, N), np.float64)
+    lib().orc_retrieval_scores(_ptr(q, _fp), _ptr(c, _fp), B, N, D, _ptr(out, _dp))
+    return out
+
+
+def retrieval_select(scores, context_tokens, chunk=512, threshold=0.3, min_tokens=4096, ratio=24):
+    """Kept chunk ids (ascending, -1 padded) [B, N], their count [B] and tokens [B]
+    from float32 scores [B, N]."""
+    s = _c(scores, np.float32)
+    B, N = s.shape
+    ct = _c(context_tokens, np.int32)
+    sel = np.zeros((B, N), np.int32)
+    ns = np.zeros(B, np.int32)
+    ts = np.zeros(B, np.int32)
+    lib().orc_retrieval_select(_ptr(s, _fp), _ptr(ct, _i32p), B, N, chunk, float(threshold),
+                               min_tokens, ratio, _ptr(sel, _i32p), _ptr(ns, _i32p), _ptr(ts, _i32p))
+    return sel, ns, ts

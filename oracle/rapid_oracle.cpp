@@ -37,6 +37,15 @@
  * Parity of the tree path-selection rule is unpinned beyond brute-force
  * enumeration of tiny trees (the pages define only the tree mask).
  *
+ * Retrieval ([RAPID] explainer and paper pages, section 3.1 "RAG settings"):
+ * the long context is cut into 512-token chunks, each embedded; a chunk's
+ * score is the cosine similarity of its embedding with the query embedding;
+ * chunks scoring below 0.3 are dropped and the top ones are kept within a
+ * retrieved-context budget of at least 4096 tokens and 1/24 of the input
+ * (reading: budget = max(4096, n / 24); chunks taken greedily in descending
+ * score, ties to the lower index, a chunk that does not fit the remaining
+ * budget is skipped; the kept chunks are returned in document order).
+ *
  * KV commit (the step after acceptance; the pages describe the verify pass's
  * cache layout -- [LongSpec] section 2.3, speculative rows after the history,
  * node i of the step at position P + i, node 0 the root -- but print no
@@ -470,6 +479,70 @@ int orc_kv_commit(uint8_t* K, uint8_t* V, int layers, int B, int Hkv, int64_t ca
         }
     }
     return bad;
+}
+
+// Cosine similarity of each chunk embedding with its sequence's query
+// embedding, in double: s = <q, c> / (|q| |c|), 0 if either vector is zero.
+// query [B, D], chunks [B, N, D], both float32.
+void orc_retrieval_scores(const float* query, const float* chunks, int B, int N, int D,
+                          double* scores) {
+    for (int b = 0; b < B; ++b) {
+        const float* q = query + (int64_t)b * D;
+        double qq = 0.0;
+        for (int k = 0; k < D; ++k) qq += (double)q[k] * q[k];
+        for (int j = 0; j < N; ++j) {
+            const float* c = chunks + ((int64_t)b * N + j) * D;
+            double qc = 0.0, cc = 0.0;
+            for (int k = 0; k < D; ++k) {
+                qc += (double)q[k] * c[k];
+                cc += (double)c[k] * c[k];
+            }
+            scores[(int64_t)b * N + j] = (qq > 0.0 && cc > 0.0) ? qc / (std::sqrt(qq) * std::sqrt(cc)) : 0.0;
+        }
+    }
+}
+
+// The retrieved context of each sequence from its chunk scores (float32, the
+// precision the decision is taken in): sequence b has n_b = context_tokens[b]
+// tokens in ceil(n_b / chunk) chunks, chunk j holding min(chunk, n_b - j chunk)
+// of them; budget_b = max(min_tokens, n_b / ratio).  Chunks are visited in
+// descending score (ties: lower index); the visit stops at the first chunk
+// below the threshold; a chunk is kept if its tokens fit what is left of the
+// budget.  selected[b][0 .. n_sel) = kept chunk ids, ascending.
+void orc_retrieval_select(const float* scores, const int32_t* context_tokens, int B, int N,
+                          int chunk, float threshold, int min_tokens, int ratio,
+                          int32_t* selected, int32_t* n_selected, int32_t* tokens_selected) {
+    for (int b = 0; b < B; ++b) {
+        const int64_t n = context_tokens[b];
+        int nc = (int)((n + chunk - 1) / chunk);
+        if (nc > N) nc = N;
+        const int64_t budget = std::max<int64_t>(min_tokens, n / ratio);
+        std::vector<int> order(nc);
+        for (int j = 0; j < nc; ++j) order[j] = j;
+        const float* s = scores + (int64_t)b * N;
+        std::sort(order.begin(), order.end(), [&](int x, int y) {
+            return s[x] > s[y] || (s[x] == s[y] && x < y);
+        });
+        std::vector<char> keep(nc, 0);
+        int64_t left = budget, used = 0;
+        int cnt = 0;
+        for (int j : order) {
+            if (!(s[j] >= threshold)) break;
+            const int64_t len = std::min<int64_t>(chunk, n - (int64_t)j * chunk);
+            if (len <= left) {
+                keep[j] = 1;
+                left -= len;
+                used += len;
+                ++cnt;
+            }
+        }
+        int w = 0;
+        for (int j = 0; j < nc; ++j)
+            if (keep[j]) selected[(int64_t)b * N + w++] = j;
+        for (int j = w; j < N; ++j) selected[(int64_t)b * N + j] = -1;
+        n_selected[b] = cnt;
+        tokens_selected[b] = (int32_t)used;
+    }
 }
 
 // The history after a committed step: the root and the accepted rows join it.
