@@ -340,6 +340,9 @@ def run_gpu(args, w):
     # ---- KV commit of an accepted path, all layers (moves the cache rows last) -
     kv_commit = kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream)
 
+    # ---- retrieval for the draft's context (once per request, not per step) -
+    retrieval = retrieval_timing(w, dev, stream)
+
     # ---- numbers -----------------------------------------------------------
     ms_per_step = total_ms / args.steps
     value = ws * args.steps / (total_ms / 1e3)
@@ -372,6 +375,7 @@ def run_gpu(args, w):
                     "d2h_bytes_per_step": d2h},
             "accept_roofline": acc_roof,
             "kv_commit": kv_commit,
+            "retrieval": retrieval,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": wall}
@@ -415,6 +419,74 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     return {"us_per_step": e0.elapsed_time(e1) / reps * 1e3, "layers": w.layers,
             "rows_moved_per_layer": w.B * w.Hkv * n, "bytes_moved": moved,
             "launches_per_step": 1}
+
+
+def retrieval_timing(w, dev, stream, D=1024, reps=20):
+    """Chunk scoring and budgeted selection for the draft's retrieved context:
+    chunks of 512 tokens of the workload's context, 1024-wide bf16 embeddings.
+    One request (device time of both calls) and a batch of requests whose
+    chunk embeddings exceed L2 (scores: algorithmic bytes = the embeddings read
+    once + the scores written, / CUDA-event time per call).  Calls are replayed
+    from a CUDA graph, so host launch cost is not in the figures."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+
+    N = -(-w.prefix // 512)
+    out = {"chunks_per_request": N, "embed_dim": D, "dtype": "bf16"}
+    g = torch.Generator().manual_seed(2024)
+
+    def run(Bq):
+        q = torch.randn((Bq, D), generator=g).to(torch.bfloat16).to(dev)
+        c = torch.randn((Bq, N, D), generator=g).to(torch.bfloat16).to(dev)
+        ctx = torch.full((Bq,), w.prefix, dtype=torch.int32, device=dev)
+        s = torch.empty((Bq, N), dtype=torch.float32, device=dev)
+        sel = torch.empty((Bq, N), dtype=torch.int32, device=dev)
+        ns = torch.empty(Bq, dtype=torch.int32, device=dev)
+        ts = torch.empty(Bq, dtype=torch.int32, device=dev)
+
+        def scores_call():
+            rapid.rapid_retrieval_scores(q, c, s)
+
+        def select_call():
+            rapid.rapid_retrieval_select(s, ctx, sel, ns, ts, threshold=-1.0)
+
+        for _ in range(3):
+            scores_call()
+            select_call()
+        torch.cuda.synchronize()
+        # each call's kernels are tiny for one request: replay a CUDA graph of
+        # `reps` calls so that the host's launch cost is not in the figure
+        out_ms = []
+        for fn in (scores_call, select_call):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(reps):
+                    fn()
+            graph.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream()
+            e0.record(cur)
+            graph.replay()
+            e1.record(cur)
+            torch.cuda.synchronize()
+            out_ms.append(e0.elapsed_time(e1) / reps)
+        assert rapid.rapid_device_error(True) == 0
+        return out_ms[0], out_ms[1], c.numel() * 2 + q.numel() * 2 + s.numel() * 4
+
+    ms_s, ms_sel, _ = run(1)
+    out["request_us"] = {"scores": ms_s * 1e3, "select": ms_sel * 1e3}
+    Bq = max(1, -(-200_000_000 // (N * D * 2)))
+    ms_s, ms_sel, nbytes = run(Bq)
+    peak, peak_src = _peaks()
+    gbs = nbytes / (ms_s * 1e-3) / 1e9
+    out["batch"] = {"requests": Bq, "scores_ms": ms_s, "select_ms": ms_sel,
+                    "scores_roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
+                                        "unit": "GB/s", "frac": gbs / peak,
+                                        "algorithmic_bytes_per_launch": nbytes}}
+    return out
 
 
 def accept_batch_roofline(w, dev, stream, reps=20):
@@ -478,6 +550,31 @@ def profile_accept(w, B):
         sys.exit(1)
 
 
+def profile_retrieval(B, N=240, D=1024):
+    """Three scores + select calls on B requests of N chunks x D bf16, no timing."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(2024)
+    q = torch.randn((B, D), generator=g).to(torch.bfloat16).to(dev)
+    c = torch.randn((B, N, D), generator=g).to(torch.bfloat16).to(dev)
+    ctx = torch.full((B,), N * 512, dtype=torch.int32, device=dev)
+    s = torch.empty((B, N), dtype=torch.float32, device=dev)
+    sel = torch.empty((B, N), dtype=torch.int32, device=dev)
+    ns = torch.empty(B, dtype=torch.int32, device=dev)
+    ts = torch.empty(B, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        rapid.rapid_retrieval_scores(q, c, s)
+        rapid.rapid_retrieval_select(s, ctx, sel, ns, ts, threshold=-1.0)
+    torch.cuda.synchronize()
+    err = rapid.rapid_device_error()
+    print(json.dumps({"profile_retrieval": B, "chunks": N, "dim": D, "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,6 +584,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="named workload (default: the 32-layer 120K Llama-3.1-8B step)")
+    ap.add_argument("--profile-retrieval", type=int, default=0, metavar="B",
+                    help="run retrieval scores + select on B requests of 240 chunks x 1024 "
+                         "(for ncu) and exit")
     ap.add_argument("--profile-accept", type=int, default=0, metavar="B",
                     help="only run rapid_accept three times on B sequences of the "
                          "workload's rows (a fixed launch sequence for ncu captures)")
@@ -497,6 +597,9 @@ def main():
         w = {x.name: x for x in wl.ALL}[args.workload]
     global WORKLOAD
     WORKLOAD = w.name
+    if args.profile_retrieval > 0:
+        profile_retrieval(args.profile_retrieval)
+        return
     if args.profile_accept > 0:
         profile_accept(w, args.profile_accept)
     elif args.impl == "reference":

@@ -233,8 +233,9 @@ int rapid_version(void);
 /*
  * Sticky error bits that kernels of this library raised on the CURRENT device
  * (bit 0: a bounded wait for an asynchronous copy gave up, so the outputs of
- * that call are invalid; bit 1: rapid_kv_commit or rapid_kv_advance found an
- * invalid device-side input and left that sequence alone).  Synchronises the device to read the word; clears it
+ * that call are invalid; bit 1: rapid_kv_commit, rapid_kv_advance or
+ * rapid_retrieval_select found an invalid device-side input and left that
+ * sequence alone).  Synchronises the device to read the word; clears it
  * when `clear` is non-zero.  Returns -1 if the word could not be read.
  */
 int rapid_device_error(int clear);
@@ -303,6 +304,60 @@ rapid_status rapid_kv_commit(void* const* K_layers, void* const* V_layers, int l
  */
 rapid_status rapid_kv_advance(int32_t* prefix_len, const int32_t* n_accepted, int B, int n_q,
                               int64_t kv_capacity, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Retrieval for the draft's compressed context                              */
+/* ------------------------------------------------------------------------ */
+
+/* Most chunks per sequence rapid_retrieval_select takes. */
+enum { RAPID_RETRIEVAL_MAX_CHUNKS = 8192 };
+
+/*
+ * Cosine similarity of every chunk embedding with its sequence's query
+ * embedding ("RAPID: Long-Context Inference with Retrieval-Augmented
+ * Speculative Decoding", section 3.1, RAG settings: the context is cut into
+ * chunks, each embedded, and chunks are ranked by cosine similarity with the
+ * query embedding):
+ *   scores[b][j] = <query[b], chunks[b][j]> / (|query[b]| |chunks[b][j]|)
+ * (0 when either vector is zero), in fp32.
+ *
+ *  query   device [B, D], chunks device [B, N, D], both of dtype
+ *          RAPID_DTYPE_F32 or RAPID_DTYPE_BF16, 16-byte aligned; D a
+ *          multiple of 8 in [8, 8192].
+ *  scores  device float [B, N].
+ * Errors: RAPID_EINVAL for NULL pointers, B < 1, N < 1, a bad D, dtype or
+ * alignment; RAPID_ECUDA on launch failure.
+ */
+rapid_status rapid_retrieval_scores(const void* query, const void* chunks, int dtype, int B, int N,
+                                    int D, float* scores, void* stream);
+
+/*
+ * The retrieved context of every sequence from its chunk scores (same
+ * section: chunks scoring below `threshold` (0.3 there) are dropped and the
+ * retrieved context stays within at least `min_tokens` (4096) tokens and
+ * 1 / `ratio` (1/24) of the input).  Reading: sequence b has n_b =
+ * context_tokens[b] tokens in ceil(n_b / chunk_tokens) chunks (chunk j holds
+ * min(chunk_tokens, n_b - j chunk_tokens)); its budget is max(min_tokens,
+ * n_b / ratio); chunks are visited in descending score (ties: lower index),
+ * the visit stops at the first chunk below the threshold, and a chunk is kept
+ * if its tokens fit what is left of the budget.
+ *
+ *  scores          device float [B, N] (entries past the sequence's chunk
+ *                  count are ignored)
+ *  context_tokens  device int32 [B]
+ *  selected        device int32 [B, N]: the kept chunk ids in ascending
+ *                  order, then -1
+ *  n_selected, tokens_selected  device int32 [B]
+ * Errors: RAPID_EINVAL for NULL pointers, B < 1, N outside [1,
+ * RAPID_RETRIEVAL_MAX_CHUNKS], chunk_tokens < 1, ratio < 1, min_tokens < 0;
+ * RAPID_ECUDA on launch failure.  A sequence whose context_tokens is negative
+ * or needs more than N chunks keeps nothing and sets bit 1 of the device
+ * error word.
+ */
+rapid_status rapid_retrieval_select(const float* scores, const int32_t* context_tokens, int B, int N,
+                                    int chunk_tokens, float threshold, int min_tokens, int ratio,
+                                    int32_t* selected, int32_t* n_selected,
+                                    int32_t* tokens_selected, void* stream);
 
 
 #ifdef __cplusplus

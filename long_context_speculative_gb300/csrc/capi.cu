@@ -7,6 +7,7 @@
 #include "attn.cuh"
 #include "common.cuh"
 #include "kv_commit.cuh"
+#include "retrieval.cuh"
 #include "rapid.h"
 
 namespace rapid {
@@ -258,6 +259,33 @@ rapid_status rapid_kv_advance(int32_t* prefix_len, const int32_t* n_accepted, in
         return RAPID_EINVAL;
     return launch_kv_advance(prefix_len, n_accepted, B, n_q, kv_capacity, device_error_word(),
                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RAPID_OK
+               : RAPID_ECUDA;
+}
+
+rapid_status rapid_retrieval_scores(const void* query, const void* chunks, int dtype, int B, int N,
+                                    int D, float* scores, void* stream) {
+    if (!query || !chunks || !scores || B < 1 || N < 1) return RAPID_EINVAL;
+    if (D < 8 || D > 8192 || D % 8 != 0) return RAPID_EINVAL;
+    if (dtype != RAPID_DTYPE_F32 && dtype != RAPID_DTYPE_BF16) return RAPID_EINVAL;
+    if (!aligned16(query) || !aligned16(chunks)) return RAPID_EINVAL;
+    return launch_retrieval_scores(query, chunks, dtype, B, N, D, scores,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RAPID_OK
+               : RAPID_ECUDA;
+}
+
+rapid_status rapid_retrieval_select(const float* scores, const int32_t* context_tokens, int B, int N,
+                                    int chunk_tokens, float threshold, int min_tokens, int ratio,
+                                    int32_t* selected, int32_t* n_selected,
+                                    int32_t* tokens_selected, void* stream) {
+    if (!scores || !context_tokens || !selected || !n_selected || !tokens_selected) return RAPID_EINVAL;
+    if (B < 1 || N < 1 || N > RAPID_RETRIEVAL_MAX_CHUNKS || chunk_tokens < 1 || ratio < 1 ||
+        min_tokens < 0)
+        return RAPID_EINVAL;
+    return launch_retrieval_select(scores, context_tokens, B, N, chunk_tokens, threshold, min_tokens,
+                                   ratio, selected, n_selected, tokens_selected, device_error_word(),
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? RAPID_OK
                : RAPID_ECUDA;
 }

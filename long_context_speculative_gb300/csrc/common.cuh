@@ -38,6 +38,35 @@ RAPID_DEVICE float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs (f32x2 arithmetic: one instruction for two lanes of work).
+// ---------------------------------------------------------------------------
+RAPID_DEVICE uint64_t pack2(float2 v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+RAPID_DEVICE float2 unpack2(uint64_t r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+RAPID_DEVICE float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(d);
+}
+RAPID_DEVICE float2 add2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+    return unpack2(d);
+}
+RAPID_DEVICE float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
+    return unpack2(d);
+}
+
+// ---------------------------------------------------------------------------
 // Philox4x32-10 counter-based generator (Salmon, Moraes, Dror, Shaw, "Parallel
 // Random Numbers: As Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64-bit
 // multiplies and xors, key advanced by two Weyl constants per round.

@@ -22,6 +22,7 @@ RAPID_ACCEPT_TAIL_CLAMP = 1
 RAPID_MAX_NQ = 64
 RAPID_MAX_VOCAB = 229376
 RAPID_COMMIT_MAX_LAYERS = 128
+RAPID_RETRIEVAL_MAX_CHUNKS = 8192
 
 _lib = None
 
@@ -67,6 +68,10 @@ def lib() -> ctypes.CDLL:
     L.rapid_kv_commit.restype = i32
     L.rapid_kv_advance.argtypes = [vp, vp, i32, i32, i64, vp]
     L.rapid_kv_advance.restype = i32
+    L.rapid_retrieval_scores.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
+    L.rapid_retrieval_scores.restype = i32
+    L.rapid_retrieval_select.argtypes = [vp, vp, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
+    L.rapid_retrieval_select.restype = i32
     _lib = L
     return L
 
@@ -178,6 +183,26 @@ def rapid_kv_advance(prefix_len, n_accepted, n_q, kv_capacity, stream=None):
     st = lib().rapid_kv_advance(_ptr(prefix_len), _ptr(n_accepted), prefix_len.shape[0], n_q,
                                 kv_capacity, _stream(stream))
     _check(st, "rapid_kv_advance")
+
+
+def rapid_retrieval_scores(query, chunks, scores, stream=None):
+    """Cosine similarities scores [B, N] of chunks [B, N, D] with query [B, D]."""
+    _need_cuda(query, chunks, scores)
+    B, N, D = chunks.shape
+    st = lib().rapid_retrieval_scores(_ptr(query), _ptr(chunks), _dtype_code(chunks), B, N, D,
+                                      _ptr(scores), _stream(stream))
+    _check(st, "rapid_retrieval_scores")
+
+
+def rapid_retrieval_select(scores, context_tokens, selected, n_selected, tokens_selected,
+                           chunk_tokens=512, threshold=0.3, min_tokens=4096, ratio=24, stream=None):
+    """Kept chunk ids (ascending, then -1) per sequence under the RAG budget."""
+    _need_cuda(scores, context_tokens, selected, n_selected, tokens_selected)
+    B, N = scores.shape
+    st = lib().rapid_retrieval_select(_ptr(scores), _ptr(context_tokens), B, N, chunk_tokens,
+                                      float(threshold), min_tokens, ratio, _ptr(selected),
+                                      _ptr(n_selected), _ptr(tokens_selected), _stream(stream))
+    _check(st, "rapid_retrieval_select")
 
 
 def rapid_device_error(clear: bool = True) -> int:

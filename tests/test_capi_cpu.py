@@ -79,6 +79,25 @@ def test_kv_commit_host_validation_without_gpu(lib):
     assert lib.rapid_kv_advance(ctypes.c_void_p(16), ctypes.c_void_p(16), 1, 65, 4096, None) == -1
 
 
+def test_retrieval_host_validation_without_gpu(lib):
+    p = ctypes.c_void_p(16)   # a fake, aligned device address (never dereferenced)
+    good = [p, p, 1, 4, 240, 1024, p, None]
+    for i, bad in [(0, None), (1, None), (2, 7), (3, 0), (4, 0), (5, 0), (5, 12), (5, 8200),
+                   (6, None)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.rapid_retrieval_scores(*args) == -1, i
+    args = list(good)
+    args[1] = ctypes.c_void_p(24)   # not 16-byte aligned
+    assert lib.rapid_retrieval_scores(*args) == -1
+    good = [p, p, 4, 240, 512, ctypes.c_float(0.3), 4096, 24, p, p, p, None]
+    for i, bad in [(0, None), (1, None), (2, 0), (3, 0), (3, 8193), (4, 0), (6, -1), (7, 0),
+                   (8, None), (9, None), (10, None)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.rapid_retrieval_select(*args) == -1, i
+
+
 def test_no_cpu_fallback_for_cpu_tensors(lib):
     import torch
     Q = torch.zeros((1, 4, 5, 128), dtype=torch.bfloat16)
