@@ -19,6 +19,8 @@ the passages it follows:
   history after the root, in path order (``kv_commit``, ``kv_advance``).
 * retrieval for the draft's compressed context: "RAPID ..." section 3.1, RAG
   settings (``retrieval_scores``, ``retrieval_select``).
+* target logits from the shared LM head: "LongSpec ..." section 2.1
+  (``lm_head_logits``).
 """
 import ctypes
 import os
@@ -78,6 +80,8 @@ def lib():
         L.orc_retrieval_select.argtypes = [_fp, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_float, ctypes.c_int, ctypes.c_int, _i32p,
                                            _i32p, _i32p]
+        L.orc_lm_head_logits.argtypes = [_fp, _fp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp,
+                                          ctypes.c_int]
         L.orc_first_token_hist.argtypes = [_fp, _fp, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, ctypes.c_int, ctypes.c_uint64,
                                            ctypes.c_int64, _i64p, ctypes.c_int]
@@ -320,3 +324,18 @@ def retrieval_select(scores, context_tokens, chunk=512, threshold=0.3, min_token
     lib().orc_retrieval_select(_ptr(s, _fp), _ptr(ct, _i32p), B, N, chunk, float(threshold),
                                min_tokens, ratio, _ptr(sel, _i32p), _ptr(ns, _i32p), _ptr(ts, _i32p))
     return sel, ns, ts
+
+
+def lm_head_logits(hidden, W, nthreads=None):
+    """Logits [rows, V] (double) of hidden states [rows, hidden_dim] against an LM
+    head W [V, hidden_dim] (float32 arrays; bf16 values pass exactly)."""
+    h = _c(hidden, np.float32)
+    w = _c(W, np.float32)
+    rows, hd = h.shape
+    V, hd2 = w.shape
+    if hd != hd2:
+        raise ValueError("hidden sizes differ")
+    out = np.zeros((rows, V), np.float64)
+    lib().orc_lm_head_logits(_ptr(h, _fp), _ptr(w, _fp), rows, hd, V, _ptr(out, _dp),
+                             nthreads or default_threads())
+    return out

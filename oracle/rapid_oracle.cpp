@@ -545,6 +545,27 @@ void orc_retrieval_select(const float* scores, const int32_t* context_tokens, in
     }
 }
 
+// Target logits of the verify rows from their final hidden states and the LM
+// head ("LongSpec: Long-Context Lossless Speculative Decoding with Efficient
+// Drafting and Verification", section 2.1: the drafter and the target share
+// the embedding and LM-head weights; "RAPID ..." section 2.1: z is the
+// target's logit vector over the vocabulary):
+//   z[r][v] = sum_k H[r][k] * W[v][k],
+// H [rows, hidden] and W [V, hidden] (one vocabulary entry per row of W, the
+// usual LM-head weight layout), summed in double.
+void orc_lm_head_logits(const float* H, const float* W, int rows, int hidden, int V, double* z,
+                        int nthreads) {
+    parallel_for(V, nthreads, [&](int64_t v) {
+        const float* w = W + v * hidden;
+        for (int r = 0; r < rows; ++r) {
+            const float* h = H + (int64_t)r * hidden;
+            double acc = 0.0;
+            for (int k = 0; k < hidden; ++k) acc += (double)h[k] * (double)w[k];
+            z[(int64_t)r * V + v] = acc;
+        }
+    });
+}
+
 // The history after a committed step: the root and the accepted rows join it.
 void orc_kv_advance(int32_t* prefix_len, const int32_t* n_acc, int B) {
     for (int b = 0; b < B; ++b) prefix_len[b] += 1 + n_acc[b];
