@@ -343,6 +343,9 @@ def run_gpu(args, w):
     # ---- retrieval for the draft's context (once per request, not per step) -
     retrieval = retrieval_timing(w, dev, stream)
 
+    # ---- target logits from the LM head, alone and followed by acceptance ---
+    lm_head = lm_head_timing(w, dev, stream)
+
     # ---- numbers -----------------------------------------------------------
     ms_per_step = total_ms / args.steps
     value = ws * args.steps / (total_ms / 1e3)
@@ -376,6 +379,7 @@ def run_gpu(args, w):
             "accept_roofline": acc_roof,
             "kv_commit": kv_commit,
             "retrieval": retrieval,
+            "lm_head_accept": lm_head,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": wall}
@@ -419,6 +423,66 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     return {"us_per_step": e0.elapsed_time(e1) / reps * 1e3, "layers": w.layers,
             "rows_moved_per_layer": w.B * w.Hkv * n, "bytes_moved": moved,
             "launches_per_step": 1}
+
+
+def lm_head_timing(w, dev, stream, hidden=4096, reps=20):
+    """rapid_lm_head and rapid_lm_head_accept for the workload's verify rows
+    (B * n_q hidden states of width 4096, a V x 4096 bf16 head: 1.05 GB for
+    the 128256-entry vocabulary, larger than L2, so every call streams it from
+    HBM).  Algorithmic bytes = W + hidden states read once + z written."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    rows = w.B * w.n_q
+    if rows > rapid.RAPID_LM_HEAD_MAX_ROWS:
+        return {"skipped": f"{rows} verify rows > {rapid.RAPID_LM_HEAD_MAX_ROWS}"}
+    g = torch.Generator(device=dev).manual_seed(4096)
+    H = torch.randn((rows, hidden), generator=g, device=dev).to(torch.bfloat16)
+    W = torch.empty((w.V, hidden), dtype=torch.bfloat16, device=dev)
+    for i in range(0, w.V, 16384):   # fill in slices to bound the fp32 temporary
+        n = min(16384, w.V - i)
+        W[i:i + n] = (torch.randn((n, hidden), generator=g, device=dev) * (3.0 / 64)).to(torch.bfloat16)
+    z = torch.empty((rows, w.V), dtype=torch.float32, device=dev)
+    inp = wl.accept_inputs(w)
+    q, tok = inp.q.to(dev), inp.tokens.to(dev)
+    par = None if inp.parent is None else inp.parent.to(dev)
+    ws = torch.empty(rapid.rapid_lm_head_accept_workspace_size(w.B, w.n_q, w.V), dtype=torch.uint8,
+                     device=dev)
+    n_acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(w.B, dtype=torch.int32, device=dev)
+
+    def fused(i):
+        rapid.rapid_lm_head_accept(H, W, q, tok, par, w.T, w.eta, i,
+                                   rapid.RAPID_ACCEPT_TAIL_CLAMP, n_acc, nxt, None, None, ws)
+
+    for i in range(3):
+        rapid.rapid_lm_head(H, W, z)
+        fused(i)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record(stream)
+    for _ in range(reps):
+        rapid.rapid_lm_head(H, W, z)
+    ev[1].record(stream)
+    for i in range(reps):
+        fused(100 + i)
+    ev[2].record(stream)
+    torch.cuda.synchronize()
+    assert rapid.rapid_device_error(True) == 0
+    ms_head = ev[0].elapsed_time(ev[1]) / reps
+    ms_fused = ev[1].elapsed_time(ev[2]) / reps
+    nbytes = W.numel() * 2 + H.numel() * 2 + z.numel() * 4
+    peak, _ = _peaks()
+    gbs = nbytes / (ms_head * 1e-3) / 1e9
+    out = {"rows": rows, "hidden": hidden, "vocab": w.V, "weight_bytes": W.numel() * 2,
+           "lm_head_us": ms_head * 1e3, "lm_head_accept_us": ms_fused * 1e3,
+           "roofline": {"bound": "hbm", "kernel": "lm_head_kernel", "achieved": gbs, "peak": peak,
+                        "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes_per_launch": nbytes}}
+    del W
+    torch.cuda.empty_cache()
+    return out
 
 
 def retrieval_timing(w, dev, stream, D=1024, reps=20):
@@ -550,6 +614,29 @@ def profile_accept(w, B):
         sys.exit(1)
 
 
+def profile_lm_head(rows=11, hidden=4096, V=128256):
+    """Three rapid_lm_head calls (11 rows x 4096 against a 128256 x 4096 bf16 head), no timing."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(4096)
+    H = torch.randn((rows, hidden), generator=g, device=dev).to(torch.bfloat16)
+    W = torch.empty((V, hidden), dtype=torch.bfloat16, device=dev)
+    for i in range(0, V, 16384):
+        n = min(16384, V - i)
+        W[i:i + n] = (torch.randn((n, hidden), generator=g, device=dev) * (3.0 / 64)).to(torch.bfloat16)
+    z = torch.empty((rows, V), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        rapid.rapid_lm_head(H, W, z)
+    torch.cuda.synchronize()
+    err = rapid.rapid_device_error()
+    print(json.dumps({"profile_lm_head": rows, "hidden": hidden, "vocab": V, "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def profile_retrieval(B, N=240, D=1024):
     """Three scores + select calls on B requests of N chunks x D bf16, no timing."""
     import torch
@@ -584,6 +671,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     help="named workload (default: the 32-layer 120K Llama-3.1-8B step)")
+    ap.add_argument("--profile-lm-head", action="store_true",
+                    help="run rapid_lm_head three times on 11 x 4096 rows against a "
+                         "128256 x 4096 head (for ncu) and exit")
     ap.add_argument("--profile-retrieval", type=int, default=0, metavar="B",
                     help="run retrieval scores + select on B requests of 240 chunks x 1024 "
                          "(for ncu) and exit")
@@ -597,6 +687,9 @@ def main():
         w = {x.name: x for x in wl.ALL}[args.workload]
     global WORKLOAD
     WORKLOAD = w.name
+    if args.profile_lm_head:
+        profile_lm_head()
+        return
     if args.profile_retrieval > 0:
         profile_retrieval(args.profile_retrieval)
         return

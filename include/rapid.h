@@ -26,11 +26,23 @@
  *                      by p where p_hat < 0.1 * max p_hat, and the adjusted
  *                      residual norm(max(p - p_hat, p - q))).
  *
+ *   rapid_kv_commit    after acceptance, the accepted path's speculative K/V
+ *   rapid_kv_advance   rows join the history next to the root, and the
+ *                      history lengths grow by 1 + n_accepted.
+ *
+ *   rapid_lm_head      the target's logits of the verify rows from the shared
+ *   rapid_lm_head_accept  LM head, alone or followed by rapid_accept.
+ *
+ *   rapid_retrieval_scores  cosine scores of chunk embeddings against the
+ *   rapid_retrieval_select  query, and the budgeted, thresholded choice of
+ *                      chunks for the draft's retrieved context ("RAPID ...",
+ *                      section 3.1, RAG settings).
+ *
  * Conventions shared by every call:
  *  - All tensor arguments are DEVICE pointers owned by the caller.  The library
  *    allocates nothing on these paths; scratch space is the caller's
  *    `workspace` (size from the matching *_workspace_size call, 256-byte
- *    aligned).  The library never writes to the KV cache.
+ *    aligned).  Only rapid_kv_commit writes to the KV cache.
  *  - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t
  *    passed as void*; NULL = the legacy default stream).  No call
  *    synchronises the device; results are valid once the stream reaches them.
@@ -358,6 +370,59 @@ rapid_status rapid_retrieval_select(const float* scores, const int32_t* context_
                                     int chunk_tokens, float threshold, int min_tokens, int ratio,
                                     int32_t* selected, int32_t* n_selected,
                                     int32_t* tokens_selected, void* stream);
+/* ------------------------------------------------------------------------ */
+/* Target logits from the shared LM head                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Limits of rapid_lm_head (rows = verify rows of one call). */
+enum {
+    RAPID_LM_HEAD_MAX_ROWS = 256,
+    RAPID_LM_HEAD_MAX_HIDDEN = 16384,
+    RAPID_LM_HEAD_MAX_VOCAB = 1 << 22
+};
+
+/*
+ * The target's logits of the verify rows from their final hidden states and
+ * the LM head ("LongSpec: Long-Context Lossless Speculative Decoding with
+ * Efficient Drafting and Verification", section 2.1: the drafter shares the
+ * target's embedding and LM-head weights; "RAPID: Long-Context Inference with
+ * Retrieval-Augmented Speculative Decoding", section 2.1: z is the target's
+ * logit vector over the vocabulary):
+ *   z[r][v] = sum_k hidden[r][k] * W_lm[v][k],   fp32 accumulation.
+ *
+ *  hidden  device bf16 [rows, hidden_dim], 16-byte aligned
+ *  W_lm    device bf16 [V, hidden_dim] (one vocabulary entry per row, the
+ *          usual LM-head weight layout), 16-byte aligned
+ *  z       device fp32 [rows, V]
+ * rows in [1, RAPID_LM_HEAD_MAX_ROWS]; hidden_dim a multiple of 64 in [64,
+ * RAPID_LM_HEAD_MAX_HIDDEN]; V in [1, RAPID_LM_HEAD_MAX_VOCAB].
+ * Errors: RAPID_EINVAL for NULL pointers, sizes out of range or misaligned
+ * pointers; RAPID_EUNSUPPORTED without the driver's tensor-map encoder;
+ * RAPID_ECUDA on launch failure.  A bounded wait inside the kernel that runs
+ * out (one second) sets bit 0 of the device error word; z is then invalid.
+ */
+rapid_status rapid_lm_head(const void* hidden, const void* W_lm, int rows, int hidden_dim, int V,
+                           float* z, void* stream);
+
+/* Bytes of scratch that rapid_lm_head_accept needs: the B * n_q * V fp32
+ * logits plus rapid_accept's scratch; 0 for unsupported sizes. */
+size_t rapid_lm_head_accept_workspace_size(int B, int n_q, int V);
+
+/*
+ * rapid_accept on logits that rapid_lm_head computes from the verify rows'
+ * hidden states [B * n_q, hidden_dim] (row b * n_q + i is node i of sequence
+ * b): the two launches run back to back on `stream`, and z lives in the
+ * workspace (for one verify step, 11 x 128256 fp32 = 5.6 MB, which stays in
+ * L2 between them), so the caller never holds the logits.  Every other
+ * argument, output and error is rapid_accept's; B * n_q is at most
+ * RAPID_LM_HEAD_MAX_ROWS and V at most RAPID_MAX_VOCAB.
+ */
+rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidden_dim,
+                                  const float* q_draft, const int32_t* draft_tokens,
+                                  const int32_t* parent, int B, int n_q, int V, float T, float eta,
+                                  uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
+                                  int32_t* next_token, int32_t* path, float* diag,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 
 #ifdef __cplusplus

@@ -7,6 +7,7 @@
 #include "attn.cuh"
 #include "common.cuh"
 #include "kv_commit.cuh"
+#include "lm_head.cuh"
 #include "retrieval.cuh"
 #include "rapid.h"
 
@@ -109,6 +110,44 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     return pl;
 }
 
+// The acceptance launch after argument checks (shared by rapid_accept and
+// rapid_lm_head_accept).
+rapid_status accept_launch(const float* z_target, const float* q_draft,
+                           const int32_t* draft_tokens, const int32_t* parent, int B, int n_q,
+                           int V, float T, float eta, uint64_t philox_seed, uint32_t flags,
+                           int32_t* n_accepted, int32_t* next_token, int32_t* path, float* diag,
+                           void* workspace, cudaStream_t st) {
+    AcceptShape sh{};
+    if (accept_plan(V, B * n_q, &sh) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RAPID_EUNSUPPORTED;
+    }
+    const size_t rows = (size_t)B * n_q;
+    char* ws = static_cast<char*>(workspace);
+    AcceptParams p{};
+    p.z = z_target; p.q = q_draft; p.tokens = draft_tokens; p.parent = parent;
+    p.ws_accept = reinterpret_cast<int32_t*>(ws);
+    ws += align_up(rows * sizeof(int32_t));
+    p.ws_stats = reinterpret_cast<float*>(ws);
+    p.diag = diag; p.n_accepted = n_accepted; p.next_token = next_token; p.path = path;
+    p.B = B; p.n_q = n_q; p.V = V;
+    p.bulk = ((V % 4) == 0 && aligned16(z_target) && aligned16(q_draft)) ? 1 : 0;
+    p.clamp = (flags & RAPID_ACCEPT_TAIL_CLAMP) ? 1 : 0;
+    p.invT = 1.0f / T;
+    p.eta = eta;
+    p.seed_lo = (uint32_t)(philox_seed & 0xffffffffu);
+    p.seed_hi = (uint32_t)(philox_seed >> 32);
+    p.err = device_error_word();
+    return launch_accept(p, sh, st) == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
+}
+
+bool lm_head_args_ok(int rows, int hidden_dim, int V) {
+    if (rows < 1 || rows > RAPID_LM_HEAD_MAX_ROWS) return false;
+    if (hidden_dim < 64 || hidden_dim > RAPID_LM_HEAD_MAX_HIDDEN || hidden_dim % 64 != 0) return false;
+    if (V < 1 || V > RAPID_LM_HEAD_MAX_VOCAB) return false;
+    return true;
+}
+
 }  // namespace
 }  // namespace rapid
 
@@ -183,31 +222,58 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft, const int
     const size_t need = rapid_accept_workspace_size(B, n_q, V);
     if (workspace_bytes < need) return RAPID_ENOMEM;
     if (reinterpret_cast<uintptr_t>(workspace) & 15u) return RAPID_EINVAL;
+    return accept_launch(z_target, q_draft, draft_tokens, parent, B, n_q, V, T, eta, philox_seed,
+                         flags, n_accepted, next_token, path, diag, workspace,
+                         static_cast<cudaStream_t>(stream));
+}
 
-    AcceptShape sh{};
-    if (accept_plan(V, B * n_q, &sh) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return RAPID_EUNSUPPORTED;
-    }
+rapid_status rapid_lm_head(const void* hidden, const void* W_lm, int rows, int hidden_dim, int V,
+                           float* z, void* stream) {
+    if (!hidden || !W_lm || !z) return RAPID_EINVAL;
+    if (!lm_head_args_ok(rows, hidden_dim, V)) return RAPID_EINVAL;
+    if (!aligned16(hidden) || !aligned16(W_lm) || (reinterpret_cast<uintptr_t>(z) & 3u))
+        return RAPID_EINVAL;
+    if (!lm_head_supported()) return RAPID_EUNSUPPORTED;
+    return launch_lm_head(hidden, W_lm, rows, hidden_dim, V, z, device_error_word(),
+                          static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RAPID_OK
+               : RAPID_ECUDA;
+}
 
-    const size_t rows = (size_t)B * n_q;
-    char* ws = static_cast<char*>(workspace);
-    AcceptParams p{};
-    p.z = z_target; p.q = q_draft; p.tokens = draft_tokens; p.parent = parent;
-    p.ws_accept = reinterpret_cast<int32_t*>(ws);
-    ws += align_up(rows * sizeof(int32_t));
-    p.ws_stats = reinterpret_cast<float*>(ws);
-    p.diag = diag; p.n_accepted = n_accepted; p.next_token = next_token; p.path = path;
-    p.B = B; p.n_q = n_q; p.V = V;
-    p.bulk = ((V % 4) == 0 && aligned16(z_target) && aligned16(q_draft)) ? 1 : 0;
-    p.clamp = (flags & RAPID_ACCEPT_TAIL_CLAMP) ? 1 : 0;
-    p.invT = 1.0f / T;
-    p.eta = eta;
-    p.seed_lo = (uint32_t)(philox_seed & 0xffffffffu);
-    p.seed_hi = (uint32_t)(philox_seed >> 32);
-    p.err = device_error_word();
-    cudaError_t e = launch_accept(p, sh, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
+size_t rapid_lm_head_accept_workspace_size(int B, int n_q, int V) {
+    const size_t acc = rapid_accept_workspace_size(B, n_q, V);
+    if (acc == 0 || (int64_t)B * n_q > RAPID_LM_HEAD_MAX_ROWS) return 0;
+    return align_up((size_t)B * n_q * V * sizeof(float)) + acc;
+}
+
+rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidden_dim,
+                                  const float* q_draft, const int32_t* draft_tokens,
+                                  const int32_t* parent, int B, int n_q, int V, float T, float eta,
+                                  uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
+                                  int32_t* next_token, int32_t* path, float* diag,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    if (!hidden || !W_lm || !q_draft || !draft_tokens || !n_accepted || !next_token || !workspace)
+        return RAPID_EINVAL;
+    if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return RAPID_EINVAL;
+    if ((int64_t)B * n_q > RAPID_LM_HEAD_MAX_ROWS || !lm_head_args_ok(B * n_q, hidden_dim, V))
+        return RAPID_EINVAL;
+    if (!(T > 0.f) || !std::isfinite(T) || !(eta >= 0.f) || !std::isfinite(eta)) return RAPID_EINVAL;
+    if ((flags & ~(uint32_t)RAPID_ACCEPT_TAIL_CLAMP) != 0) return RAPID_EINVAL;
+    if (!aligned16(hidden) || !aligned16(W_lm) || (reinterpret_cast<uintptr_t>(q_draft) & 3u) ||
+        !aligned16(workspace))
+        return RAPID_EINVAL;
+    if (workspace_bytes < rapid_lm_head_accept_workspace_size(B, n_q, V)) return RAPID_ENOMEM;
+    if (!lm_head_supported()) return RAPID_EUNSUPPORTED;
+    // z lives at the front of the workspace (B n_q V floats, L2-resident at
+    // the sizes of one verify step); the acceptance scratch follows it.
+    float* z = static_cast<float*>(workspace);
+    void* acc_ws = static_cast<char*>(workspace) + align_up((size_t)B * n_q * V * sizeof(float));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_lm_head(hidden, W_lm, B * n_q, hidden_dim, V, z, device_error_word(), st) !=
+        cudaSuccess)
+        return RAPID_ECUDA;
+    return accept_launch(z, q_draft, draft_tokens, parent, B, n_q, V, T, eta, philox_seed, flags,
+                         n_accepted, next_token, path, diag, acc_ws, st);
 }
 
 const char* rapid_status_string(int status) {

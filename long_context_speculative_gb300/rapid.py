@@ -23,6 +23,7 @@ RAPID_MAX_NQ = 64
 RAPID_MAX_VOCAB = 229376
 RAPID_COMMIT_MAX_LAYERS = 128
 RAPID_RETRIEVAL_MAX_CHUNKS = 8192
+RAPID_LM_HEAD_MAX_ROWS = 256
 
 _lib = None
 
@@ -72,6 +73,13 @@ def lib() -> ctypes.CDLL:
     L.rapid_retrieval_scores.restype = i32
     L.rapid_retrieval_select.argtypes = [vp, vp, i32, i32, i32, f32, i32, i32, vp, vp, vp, vp]
     L.rapid_retrieval_select.restype = i32
+    L.rapid_lm_head.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+    L.rapid_lm_head.restype = i32
+    L.rapid_lm_head_accept_workspace_size.argtypes = [i32, i32, i32]
+    L.rapid_lm_head_accept_workspace_size.restype = ctypes.c_size_t
+    L.rapid_lm_head_accept.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32,
+                                       vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.rapid_lm_head_accept.restype = i32
     _lib = L
     return L
 
@@ -156,6 +164,34 @@ def rapid_accept_noalloc(z_target, q_draft, draft_tokens, parent, T, eta, philox
                                     _ptr(n_accepted), _ptr(next_token), _ptr(path), _ptr(diag),
                                     _stream(stream))
     _check(st, "rapid_accept_noalloc")
+
+
+def rapid_lm_head(hidden, W_lm, z, stream=None):
+    """Logits z [rows, V] (fp32) of hidden [rows, hidden_dim] against W_lm [V, hidden_dim] (bf16)."""
+    _need_cuda(hidden, W_lm, z)
+    rows, hd = hidden.shape
+    V = W_lm.shape[0]
+    st = lib().rapid_lm_head(_ptr(hidden), _ptr(W_lm), rows, hd, V, _ptr(z), _stream(stream))
+    _check(st, "rapid_lm_head")
+
+
+def rapid_lm_head_accept_workspace_size(B, n_q, V):
+    return int(lib().rapid_lm_head_accept_workspace_size(B, n_q, V))
+
+
+def rapid_lm_head_accept(hidden, W_lm, q_draft, draft_tokens, parent, T, eta, philox_seed, flags,
+                         n_accepted, next_token, path, diag, workspace, stream=None):
+    """rapid_accept on the logits of hidden [B*n_q, hidden_dim] against W_lm [V, hidden_dim]."""
+    _need_cuda(hidden, W_lm, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag,
+               workspace)
+    B, n_q, V = q_draft.shape
+    st = lib().rapid_lm_head_accept(_ptr(hidden), _ptr(W_lm), hidden.shape[1], _ptr(q_draft),
+                                    _ptr(draft_tokens), _ptr(parent), B, n_q, V, float(T),
+                                    float(eta), int(philox_seed) & ((1 << 64) - 1), int(flags),
+                                    _ptr(n_accepted), _ptr(next_token), _ptr(path), _ptr(diag),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check(st, "rapid_lm_head_accept")
 
 
 def rapid_kv_commit(K_layers, V_layers, prefix_len, path, n_accepted, stream=None):
@@ -259,4 +295,24 @@ def accept(z, q, tokens, parent=None, T=1.0, eta=1.0, seed=0, tail_clamp=True, w
     flags = RAPID_ACCEPT_TAIL_CLAMP if tail_clamp else 0
     rapid_accept(z, q, tokens, parent, T, eta, seed, flags, n_acc, nxt, path, diag, workspace,
                  stream)
+    return dict(n_accepted=n_acc, next_token=nxt, path=path, diag=diag)
+
+
+def lm_head_accept(hidden, W_lm, q, tokens, parent=None, T=1.0, eta=1.0, seed=0, tail_clamp=True,
+                   want_path=True, want_diag=True, workspace=None, stream=None):
+    """accept() on the logits of the verify rows' hidden states [B*n_q, hidden_dim]."""
+    B, n_q, V = q.shape
+    dev = q.device
+    n_acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, n_q), dtype=torch.int32, device=dev) if want_path else None
+    diag = torch.empty((B, n_q, 5), dtype=torch.float32, device=dev) if want_diag else None
+    if workspace is None:
+        nbytes = rapid_lm_head_accept_workspace_size(B, n_q, V)
+        if nbytes == 0:
+            raise RapidError("unsupported lm_head_accept shape")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    flags = RAPID_ACCEPT_TAIL_CLAMP if tail_clamp else 0
+    rapid_lm_head_accept(hidden, W_lm, q, tokens, parent, T, eta, seed, flags, n_acc, nxt, path,
+                         diag, workspace, stream)
     return dict(n_accepted=n_acc, next_token=nxt, path=path, diag=diag)

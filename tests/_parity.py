@@ -37,12 +37,17 @@ def _parents(par, b, n_q):
     return [-1] + [int(x) for x in par[b][1:]]
 
 
-def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref):
+def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref, prob_rtol=PROB_RTOL,
+                 exempt=EXEMPT):
     """Compare one rapid_accept call with oracle.accept on the same inputs.
 
     gpu: dict of numpy arrays (n_accepted, next_token, path, diag) from the CUDA path.
     ref: dict from oracle.accept.  Returns a dict of exemption counts.
+    prob_rtol / exempt widen the probability tolerance and the near-boundary
+    bands when the GPU's logits themselves carry an error (the fused LM-head
+    path): a softmax moves by at most 2 max|dz| / T in relative terms.
     """
+    EXEMPT = exempt
     B, n_q, V = z.shape
     stats = dict(ratio_exempt=0, clamp_exempt=0, cdf_exempt=0, compared=0)
     for b in range(B):
@@ -63,10 +68,10 @@ def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref):
                 exempt_nodes.add(i)
                 continue
             # p(t), p_hat(t), q(t): relative 1e-5
-            np.testing.assert_allclose(dg[i, :3], dr[i, :3], rtol=PROB_RTOL, atol=1e-30,
+            np.testing.assert_allclose(dg[i, :3], dr[i, :3], rtol=prob_rtol, atol=1e-30,
                                        err_msg=f"b={b} node={i} probs")
             if np.isfinite(dr[i, 3]):
-                np.testing.assert_allclose(dg[i, 3], dr[i, 3], rtol=PROB_RTOL,
+                np.testing.assert_allclose(dg[i, 3], dr[i, 3], rtol=prob_rtol,
                                            err_msg=f"b={b} node={i} ratio")
             else:
                 assert not np.isfinite(dg[i, 3])

@@ -98,6 +98,33 @@ def test_retrieval_host_validation_without_gpu(lib):
         assert lib.rapid_retrieval_select(*args) == -1, i
 
 
+def test_lm_head_host_validation_without_gpu(lib):
+    p = ctypes.c_void_p(16)   # a fake, aligned device address (never dereferenced)
+    good = [p, p, 11, 4096, 128256, p, None]
+    for i, bad in [(0, None), (1, None), (2, 0), (2, 257), (3, 0), (3, 100), (3, 16448),
+                   (4, 0), (4, (1 << 22) + 1), (5, None)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.rapid_lm_head(*args) == -1, i
+    args = list(good)
+    args[1] = ctypes.c_void_p(24)   # W not 16-byte aligned
+    assert lib.rapid_lm_head(*args) == -1
+    assert lib.rapid_lm_head_accept_workspace_size(1, 11, 128256) >= 11 * 128256 * 4
+    assert lib.rapid_lm_head_accept_workspace_size(5, 64, 1000) == 0   # 320 rows > 256
+    ws = lib.rapid_lm_head_accept_workspace_size(1, 11, 128256)
+    good = [p, p, 4096, p, p, None, 1, 11, 128256, ctypes.c_float(1.0), ctypes.c_float(1.0), 7,
+            1, p, p, None, None, p, ws, None]
+    for i, bad in [(0, None), (1, None), (2, 96), (3, None), (4, None), (6, 0), (7, 65),
+                   (8, 229377), (9, ctypes.c_float(0.0)), (10, ctypes.c_float(-1.0)), (12, 8),
+                   (13, None), (14, None), (17, None)]:
+        args = list(good)
+        args[i] = bad
+        assert lib.rapid_lm_head_accept(*args) == -1, i
+    args = list(good)
+    args[18] = ws - 1
+    assert lib.rapid_lm_head_accept(*args) == -3   # workspace too small
+
+
 def test_no_cpu_fallback_for_cpu_tensors(lib):
     import torch
     Q = torch.zeros((1, 4, 5, 128), dtype=torch.bfloat16)
