@@ -624,6 +624,12 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     const int n = n64 > 0 ? (int)n64 : 0;
     const float* zr = p.z + row * p.V + lo;
     const float* qr = p.q + row * p.V + lo;
+    // the slice of row e starts its trip to L2 in two bulk requests, so the
+    // loads below wait for L2 rather than for DRAM one round trip at a time
+    if (t == 0 && p.bulk && n > 0) {
+        bulk_prefetch_l2(zr, (uint32_t)n * 4u);
+        if (s_has_children) bulk_prefetch_l2(qr, (uint32_t)n * 4u);
+    }
 
     // The residual if e has children, else p; p also when the residual has no
     // mass in any slice.
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
             const float4* z4 = reinterpret_cast<const float4*>(zr);
             const float4* q4 = reinterpret_cast<const float4*>(qr);
             float4* w4 = reinterpret_cast<float4*>(sw);
-#pragma unroll 2
+#pragma unroll 4
             for (int k = t; k < n / 4; k += kST) {
                 const float4 a = z4[k];
                 float4 w;
