@@ -16,11 +16,16 @@
 // M128 x N accumulator in tensor memory and W streams through shared memory
 // exactly once.
 //
-// CTA (persistent, one per SM, a contiguous run of vocabulary tiles); 192
-// threads:
-//   warp 0     TMA producer: per 64-wide hidden block, a 128 x 64 box of W
-//              (16 KB) and an N x 64 box of H (rows past the last are zero-
-//              filled by the copy) into a ring of up to 12 stages.
+// CTA (persistent, one per SM): a contiguous run of vocabulary rows, cut in
+// 16-row units so that every SM gets the same share to within 16 rows
+// (whole 128-row tiles would leave the last wave 6 % short of full); the run
+// is taken as 128-row tiles, the last one possibly shorter (a multiple of 16
+// rows, loaded as up to three smaller boxes; the MMA still computes 128 rows and the rows
+// past the run are not stored).  192 threads:
+//   warp 0     TMA producer: per 64-wide hidden block, the tile's rows of W
+//              (one 128 x 64 box, 16 KB, or boxes of 64, 32, 16 rows) and an
+//              N x 64 box of H (rows past the last are zero-filled by the
+//              copy) into a ring of up to 12 stages.
 //   warp 1     allocates tensor memory and issues the MMAs (one thread):
 //              four M128 N K16 products per stage into one of two
 //              accumulator buffers, alternating by tile.
@@ -40,6 +45,7 @@ namespace rapid {
 namespace {
 
 constexpr int kVT = 128;                    // vocabulary rows per tile (MMA M)
+constexpr int kVU = 16;                     // vocabulary rows per scheduling unit
 constexpr int kKB = 64;                     // hidden elements per stage (128 bytes of bf16)
 constexpr int kWBytes = kVT * kKB * 2;      // 16 KB of W per stage
 constexpr int kThreadsLm = 192;
@@ -82,18 +88,21 @@ enum : unsigned int {
 
 template <int N>
 __global__ void __launch_bounds__(kThreadsLm, 1)
-lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
-               int rows, int hidden, int V, float* __restrict__ z, unsigned int* err) {
+lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW64,
+               const __grid_constant__ CUtensorMap tmW32, const __grid_constant__ CUtensorMap tmW16,
+               const __grid_constant__ CUtensorMap tmH, int rows, int hidden, int V,
+               float* __restrict__ z, unsigned int* err) {
     using L = LmPlan<N>;
     constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     LmBars* bars = reinterpret_cast<LmBars*>(smem + L::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = (V + kVT - 1) / kVT;
-    const int t_begin = (int)((int64_t)tiles * blockIdx.x / gridDim.x);
-    const int t_end = (int)((int64_t)tiles * (blockIdx.x + 1) / gridDim.x);
-    const int n_tiles = t_end - t_begin;
+    // this CTA's vocabulary rows [v_begin, v_end), in whole 16-row units
+    const int units = (V + kVU - 1) / kVU;
+    const int v_begin = (int)((int64_t)units * blockIdx.x / gridDim.x) * kVU;
+    const int v_end = (int)((int64_t)units * (blockIdx.x + 1) / gridDim.x) * kVU;
+    const int n_tiles = (v_end - v_begin + kVT - 1) / kVT;
     const int kb_n = hidden / kKB;
 
     if (threadIdx.x == 0) {
@@ -129,7 +138,8 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
             int it = 0, issued = 0;
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {
-                const int y = (t_begin + j) * kVT;
+                const int y = v_begin + j * kVT;
+                const int h = v_end - y < kVT ? v_end - y : kVT;   // rows of this tile, 16 | h
                 for (int kb = 0; kb < kb_n; ++kb, ++it) {
                     const int st = it % S;
                     if (it >= S && !mbar_wait_sleep(&bars->empty[st], ((it / S) + 1) & 1, err,
@@ -142,8 +152,25 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                         break;
                     }
                     uint8_t* stage = smem + st * L::kStageBytes;
-                    mbar_arrive_expect_tx(&bars->full[st], L::kStageBytes);
-                    tma_load_2d(stage, &tmW, kb * kKB, y, &bars->full[st]);
+                    mbar_arrive_expect_tx(&bars->full[st], (uint32_t)(h * kKB * 2 + L::kHBytes));
+                    if (h == kVT) {
+                        tma_load_2d(stage, &tmW, kb * kKB, y, &bars->full[st]);
+                    } else {
+                        // a shorter tile as at most three boxes of 64, 32 and 16
+                        // rows, each landing where those rows of a full box would
+                        // (whole 1024-byte swizzle atoms: the same layout)
+                        int u = 0;
+                        if (h & 64) {
+                            tma_load_2d(stage, &tmW64, kb * kKB, y, &bars->full[st]);
+                            u += 64;
+                        }
+                        if (h & 32) {
+                            tma_load_2d(stage + u * kKB * 2, &tmW32, kb * kKB, y + u, &bars->full[st]);
+                            u += 32;
+                        }
+                        if (h & 16)
+                            tma_load_2d(stage + u * kKB * 2, &tmW16, kb * kKB, y + u, &bars->full[st]);
+                    }
                     tma_load_2d(stage + kWBytes, &tmH, kb * kKB, 0, &bars->full[st]);
                     ++issued;
                 }
@@ -208,13 +235,15 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                 break;
             }
             tc_fence_after();
-            const int v = (t_begin + j) * kVT + q4 * 32 + lane;
+            const int y = v_begin + j * kVT;
+            const int v = y + q4 * 32 + lane;
+            const bool mine = v < V && v < v_end;   // rows past the run belong to the next CTA
 #pragma unroll 1
             for (int c0 = 0; c0 < N; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(lane_addr + (uint32_t)(buf * N + c0), r);
                 tmem_wait_ld();
-                if (v < V) {
+                if (mine) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (c0 + i < rows) z[(int64_t)(c0 + i) * V + v] = __uint_as_float(r[i]);
@@ -263,18 +292,21 @@ int sm_count_lm() {
 template <int N>
 cudaError_t launch_n(const void* hidden, const void* W, int rows, int hidden_dim, int V, float* z,
                      unsigned int* err, cudaStream_t st) {
-    CUtensorMap tmW, tmH;
+    CUtensorMap tmW, tmW64, tmW32, tmW16, tmH;
     if (!make_map(&tmW, W, (uint64_t)hidden_dim, (uint64_t)V, kVT) ||
+        !make_map(&tmW64, W, (uint64_t)hidden_dim, (uint64_t)V, 64) ||
+        !make_map(&tmW32, W, (uint64_t)hidden_dim, (uint64_t)V, 32) ||
+        !make_map(&tmW16, W, (uint64_t)hidden_dim, (uint64_t)V, kVU) ||
         !make_map(&tmH, hidden, (uint64_t)hidden_dim, (uint64_t)rows, N))
         return cudaErrorInvalidValue;
     auto kern = lm_head_kernel<N>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          LmPlan<N>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int tiles = (V + kVT - 1) / kVT;
+    const int units = (V + kVU - 1) / kVU;
     const int sms = sm_count_lm();
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles < sms ? tiles : sms, 1, 1);
+    cfg.gridDim = dim3(units < sms ? units : sms, 1, 1);
     cfg.blockDim = dim3(kThreadsLm, 1, 1);
     cfg.dynamicSmemBytes = LmPlan<N>::kSmemBytes;
     cfg.stream = st;
@@ -283,7 +315,8 @@ cudaError_t launch_n(const void* hidden, const void* W, int rows, int hidden_dim
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmW, tmH, rows, hidden_dim, V, z, err);
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmW64, tmW32, tmW16, tmH, rows, hidden_dim, V, z,
+                              err);
 }
 
 }  // namespace
