@@ -334,8 +334,12 @@ def run_gpu(args, w):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
-    # ---- acceptance bandwidth on a batch larger than L2 -----------------------
+    # ---- acceptance bandwidth on batches larger than L2 ----------------------
     acc_roof = accept_batch_roofline(w, dev, stream)
+    # and on the tree configuration's own step (4 x 32 rows of 152064 entries)
+    acc_tree = None
+    if not w.tree:
+        acc_tree = accept_batch_roofline(wl.QWEN7B_TREE, dev, stream, B=wl.QWEN7B_TREE.B)
 
     # ---- KV commit of an accepted path, all layers (moves the cache rows last) -
     kv_commit = kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream)
@@ -377,6 +381,7 @@ def run_gpu(args, w):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "accept_roofline": acc_roof,
+            "accept_roofline_tree": acc_tree,
             "kv_commit": kv_commit,
             "retrieval": retrieval,
             "lm_head_accept": lm_head,
@@ -553,18 +558,23 @@ def retrieval_timing(w, dev, stream, D=1024, reps=20):
     return out
 
 
-def accept_batch_roofline(w, dev, stream, reps=20):
-    """rapid_accept alone on a batch of at least 100 MB of z + q (16 sequences of
-    the workload's chain shape, larger than L2): algorithmic bytes = 8 B per
-    vocabulary entry (z and q read once) / CUDA-event time per call."""
+def accept_batch_roofline(w, dev, stream, reps=20, B=None):
+    """rapid_accept alone on a batch of at least 100 MB of z + q (larger than L2):
+    the workload's own batch when that is large enough (the 4-sequence tree of
+    the Qwen shape: 155.7 MB), else 16 sequences of its rows, more if that stays
+    under 100 MB.  Algorithmic bytes = 8 B per vocabulary entry (z and q read
+    once) / CUDA-event time per call."""
     import torch
 
     from long_context_speculative_gb300 import rapid
     from long_context_speculative_gb300 import workloads as wl
 
-    # 16 independent sequences of the workload's rows, more if that stays under
-    # 100 MB (so that the batch is larger than L2)
-    Bb = max(16, -(-100_000_000 // (w.n_q * w.V * 8)))
+    if B is not None:
+        Bb = B
+    elif w.B * w.n_q * w.V * 8 >= 100_000_000:
+        Bb = w.B
+    else:
+        Bb = max(16, -(-100_000_000 // (w.n_q * w.V * 8)))
     inp = wl.accept_inputs(w, B=Bb, parents=None if not w.tree else None)
     z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
     par = None if inp.parent is None else inp.parent.to(dev)

@@ -335,6 +335,9 @@ accept_rows_kernel(const AcceptParams p) {
     }
     cluster.sync();   // barriers and padding in place before any copy or peer send
     griddep_wait();
+    // the selection kernel may be scheduled now: its CTAs cannot share an SM
+    // with this kernel's, so they take idle SMs and wait in griddep_wait()
+    // for this grid to finish, with their launch already behind them
 
     float* zb = bufs + (size_t)g * 2 * span;   // this group's row buffer
     float* qb = zb + span;
@@ -557,6 +560,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     __shared__ float s_tin, s_tw;
     __shared__ float s_seg[kSW];
     __shared__ float s_total[2];   // this slice's weight total; the cluster's
+    __shared__ float4 s_stats[kAcceptMaxNq];   // every row's (m1, s1, m2, s2), read up front
 
     const int cs = (int)cluster.block_rank();   // vocabulary slice
     const int b = blockIdx.y;
@@ -568,6 +572,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
         s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
         s_par[t] = t == 0 ? -1 : parent_of(p, b, t);
         s_kids[t] = 0;
+        s_stats[t] = reinterpret_cast<const float4*>(p.ws_stats)[(int64_t)b * n_q + t];
     }
     __syncthreads();
     if (t > 0 && t < n_q) s_kids[s_par[t]] = 1;   // every writer stores the same value
@@ -615,7 +620,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
 
     const int e = s_e;
     const int64_t row = (int64_t)b * n_q + e;
-    const float4 sts = reinterpret_cast<const float4*>(p.ws_stats)[row];
+    const float4 sts = s_stats[e];
     const float m1 = sts.x, inv_s1 = 1.f / sts.y, m2 = sts.z, inv_s2 = 1.f / sts.w;
     const float thr = p.clamp ? 0.1f * inv_s2 : -1.0f;   // max p_hat = 1 / s2
     const int64_t lo = (int64_t)cs * p.chunk;
