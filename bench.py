@@ -31,6 +31,22 @@ SRC_FILES_TRAFFIC = ["long_context_speculative_gb300/csrc/attn_tc.cu",
                      "long_context_speculative_gb300/csrc/attn.cuh"]
 
 
+def max_over_ranks(dist, ms, device):
+    """The slowest replica's time: the largest of every rank's `ms` (all ranks
+    get it).  With no process group, `ms` itself."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world_size, steps, ms):
+    """Steps of all replicas per second when each ran `steps` in at most `ms`."""
+    return world_size * steps / (ms / 1e3)
+
+
 def _dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -285,10 +301,7 @@ def run_gpu(args, w):
     for s in range(args.steps):
         for layer in range(w.layers):
             attn_ms.append(evs[s][layer].elapsed_time(evs[s][layer + 1]))
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, total_ms, dev)
     assert rapid.rapid_device_error(True) == 0
 
     # ---- e2e through the public API with host buffers -------------------------
@@ -328,11 +341,7 @@ def run_gpu(args, w):
         e2e_step(0x5EED0000 + s)
     e_end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(dist, e_start.elapsed_time(e_end), dev)
 
     # ---- acceptance bandwidth on batches larger than L2 ----------------------
     acc_roof = accept_batch_roofline(w, dev, stream)
@@ -352,8 +361,8 @@ def run_gpu(args, w):
 
     # ---- numbers -----------------------------------------------------------
     ms_per_step = total_ms / args.steps
-    value = ws * args.steps / (total_ms / 1e3)
-    e2e_value = ws * args.steps / (e2e_ms / 1e3)
+    value = whole_job_rate(ws, args.steps, total_ms)
+    e2e_value = whole_job_rate(ws, args.steps, e2e_ms)
     kv_rows = int(prefix_len.sum().item()) + w.B * w.n_q
     kv_bytes = 2 * w.Hkv * kv_rows * w.d * 2
     qo_bytes = 2 * w.B * w.Hq * w.n_q * w.d * 2 + w.B * w.Hq * w.n_q * 4
