@@ -28,7 +28,9 @@ UNIT = "verify_steps/s"
 WORKLOAD = "llama3.1-8b_32layers_120k"
 SRC_FILES_TRAFFIC = ["long_context_speculative_gb300/csrc/attn_tc.cu",
                      "long_context_speculative_gb300/csrc/attn_simt.cu",
-                     "long_context_speculative_gb300/csrc/attn.cuh"]
+                     "long_context_speculative_gb300/csrc/attn.cuh",
+                     "long_context_speculative_gb300/csrc/tcgen05.cuh",
+                     "long_context_speculative_gb300/csrc/common.cuh"]
 
 
 def max_over_ranks(dist, ms, device):
@@ -424,7 +426,10 @@ def run_gpu(args, w):
 def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     """rapid_kv_commit over every layer for an accepted path that moves rows
     (nodes 2, 4, 6, ...: every destination differs from its source).  The
-    moved bytes are tiny, so this is a latency figure, not a bandwidth one."""
+    moved bytes are tiny, so this is a latency figure, not a bandwidth one:
+    through the Python binding call by call (which builds the host arrays of
+    layer pointers every time), and as device time from a CUDA graph of the
+    same calls."""
     import torch
 
     from long_context_speculative_gb300 import rapid
@@ -435,19 +440,36 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
         path[:, :n] = torch.arange(2, 2 * n + 1, 2, dtype=torch.int32)
     path = path.to(dev)
     n_acc = torch.full((w.B,), n, dtype=torch.int32, device=dev)
-    for _ in range(3):
+
+    def call():
         rapid.rapid_kv_commit(Ks, Vs, prefix_len, path, n_acc)
+
+    for _ in range(3):
+        call()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
-        rapid.rapid_kv_commit(Ks, Vs, prefix_len, path, n_acc)
+        call()
     e1.record(stream)
     torch.cuda.synchronize()
+    eager_us = e0.elapsed_time(e1) / reps * 1e3
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            call()
+    graph.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    graph.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    graph_us = e0.elapsed_time(e1) / reps * 1e3
     assert rapid.rapid_device_error(True) == 0
     moved = w.layers * w.B * w.Hkv * n * w.d * 2 * 2   # K and V rows, bf16
-    return {"us_per_step": e0.elapsed_time(e1) / reps * 1e3, "layers": w.layers,
+    return {"us_per_step": eager_us, "us_per_step_graph": graph_us, "layers": w.layers,
             "rows_moved_per_layer": w.B * w.Hkv * n, "bytes_moved": moved,
             "launches_per_step": 1}
 
