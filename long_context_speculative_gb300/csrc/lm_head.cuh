@@ -6,14 +6,13 @@
 
 namespace rapid {
 
-constexpr int kLmMaxRows = 256;   // rows of one launch (the MMA's N, padded to 16..256)
-
 // True when the driver's tensor-map encoder is available.
 bool lm_head_supported();
 
 // z[r][v] = sum_k hidden[r][k] * W[v][k] for r < rows, v < V; hidden [rows,
-// hidden_dim] and W [V, hidden_dim] bf16, z [rows, V] fp32.  hidden_dim a
-// multiple of 64; hidden, W 16-byte aligned.
+// hidden_dim] and W [V, hidden_dim] bf16, z [rows, V] fp32.  rows <= 256 (the
+// MMA's N, padded to 16..256), hidden_dim a multiple of 64; hidden, W 16-byte
+// aligned.
 cudaError_t launch_lm_head(const void* hidden, const void* W, int rows, int hidden_dim, int V,
                            float* z, unsigned int* err, cudaStream_t st);
 
