@@ -427,9 +427,8 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     """rapid_kv_commit over every layer for an accepted path that moves rows
     (nodes 2, 4, 6, ...: every destination differs from its source).  The
     moved bytes are tiny, so this is a latency figure, not a bandwidth one:
-    through the Python binding call by call (which builds the host arrays of
-    layer pointers every time), and as device time from a CUDA graph of the
-    same calls."""
+    through the Python binding call by call (a KVLayerTable packs the layer
+    pointers once), and as device time from a CUDA graph of the same calls."""
     import torch
 
     from long_context_speculative_gb300 import rapid
@@ -441,8 +440,10 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     path = path.to(dev)
     n_acc = torch.full((w.B,), n, dtype=torch.int32, device=dev)
 
+    table = rapid.KVLayerTable(Ks, Vs)
+
     def call():
-        rapid.rapid_kv_commit(Ks, Vs, prefix_len, path, n_acc)
+        table.commit(prefix_len, path, n_acc)
 
     for _ in range(3):
         call()

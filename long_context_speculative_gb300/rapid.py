@@ -194,23 +194,46 @@ def rapid_lm_head_accept(hidden, W_lm, q_draft, draft_tokens, parent, T, eta, ph
     _check(st, "rapid_lm_head_accept")
 
 
+class KVLayerTable:
+    """The device addresses of every layer's K and V cache, checked and packed
+    once, for repeated rapid_kv_commit calls on the same caches (the per-call
+    packing of a few dozen pointers otherwise costs tens of microseconds of
+    host time)."""
+
+    def __init__(self, K_layers, V_layers):
+        if len(K_layers) != len(V_layers) or not K_layers:
+            raise RapidError("rapid_kv_commit needs matching, non-empty K and V layer lists")
+        if len(K_layers) > RAPID_COMMIT_MAX_LAYERS:
+            raise RapidError(f"at most {RAPID_COMMIT_MAX_LAYERS} layers per call")
+        _need_cuda(*K_layers, *V_layers)
+        shape, dtype = tuple(K_layers[0].shape), K_layers[0].dtype
+        for t in list(K_layers) + list(V_layers):
+            if tuple(t.shape) != shape or t.dtype != dtype:
+                raise RapidError("every layer's K and V cache needs the same shape and dtype")
+        self.layers = len(K_layers)
+        self.B, self.Hkv, self.cap, self.d = shape
+        self.dtype = _dtype_code(K_layers[0])
+        self._k = (ctypes.c_void_p * self.layers)(*[t.data_ptr() for t in K_layers])
+        self._v = (ctypes.c_void_p * self.layers)(*[t.data_ptr() for t in V_layers])
+        self._keep = (list(K_layers), list(V_layers))   # the caches outlive the table
+
+    def commit(self, prefix_len, path, n_accepted, stream=None):
+        st = lib().rapid_kv_commit(ctypes.cast(self._k, ctypes.c_void_p),
+                                   ctypes.cast(self._v, ctypes.c_void_p), self.layers, self.dtype,
+                                   self.B, self.Hkv, self.d, self.cap, path.shape[1],
+                                   _ptr(prefix_len), _ptr(path), _ptr(n_accepted), _stream(stream))
+        _check(st, "rapid_kv_commit")
+
+
 def rapid_kv_commit(K_layers, V_layers, prefix_len, path, n_accepted, stream=None):
     """Move the accepted speculative K/V rows of every layer next to the root.
 
     K_layers, V_layers: sequences of [B, Hkv, kv_capacity, d] caches (one per
-    layer); prefix_len [B], path [B, n_q], n_accepted [B] int32 on the device."""
-    if len(K_layers) != len(V_layers) or not K_layers:
-        raise RapidError("rapid_kv_commit needs matching, non-empty K and V layer lists")
-    _need_cuda(*K_layers, *V_layers, prefix_len, path, n_accepted)
-    B, Hkv, cap, d = K_layers[0].shape
-    n_q = path.shape[1]
-    layers = len(K_layers)
-    karr = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in K_layers])
-    varr = (ctypes.c_void_p * layers)(*[t.data_ptr() for t in V_layers])
-    st = lib().rapid_kv_commit(ctypes.cast(karr, ctypes.c_void_p), ctypes.cast(varr, ctypes.c_void_p),
-                               layers, _dtype_code(K_layers[0]), B, Hkv, d, cap, n_q,
-                               _ptr(prefix_len), _ptr(path), _ptr(n_accepted), _stream(stream))
-    _check(st, "rapid_kv_commit")
+    layer), or K_layers a KVLayerTable and V_layers None; prefix_len [B],
+    path [B, n_q], n_accepted [B] int32 on the device."""
+    _need_cuda(prefix_len, path, n_accepted)
+    table = K_layers if isinstance(K_layers, KVLayerTable) else KVLayerTable(K_layers, V_layers)
+    table.commit(prefix_len, path, n_accepted, stream)
 
 
 def rapid_kv_advance(prefix_len, n_accepted, n_q, kv_capacity, stream=None):

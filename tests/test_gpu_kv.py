@@ -30,13 +30,16 @@ def _np(ts):
     return a.numpy().copy()
 
 
-def _commit_both(K, V, P, path, n_acc):
+def _commit_both(K, V, P, path, n_acc, table=False):
     Kd = [k.to(DEV) for k in K]
     Vd = [v.to(DEV) for v in V]
     Pd = torch.as_tensor(P, dtype=torch.int32, device=DEV)
     pathd = torch.as_tensor(path, dtype=torch.int32, device=DEV)
     nd = torch.as_tensor(n_acc, dtype=torch.int32, device=DEV)
-    rapid.rapid_kv_commit(Kd, Vd, Pd, pathd, nd)
+    if table:
+        rapid.rapid_kv_commit(rapid.KVLayerTable(Kd, Vd), None, Pd, pathd, nd)
+    else:
+        rapid.rapid_kv_commit(Kd, Vd, Pd, pathd, nd)
     torch.cuda.synchronize()
     Ko, Vo = _np(K), _np(V)
     bad = oracle.kv_commit(Ko, Vo, np.asarray(P, np.int32), np.asarray(path, np.int32),
@@ -73,7 +76,7 @@ def test_tree_paths_bit_exact(dtype, d):
     P[0] = 0
     P[1] = cap - n_q            # the speculative rows end at the last cache row
     path, n_acc = _random_paths(rng, B, n_q)
-    Kg, Vg, Ko, Vo, bad = _commit_both(K, V, P, path, n_acc)
+    Kg, Vg, Ko, Vo, bad = _commit_both(K, V, P, path, n_acc, table=(d == 64))
     assert bad == 0
     assert np.array_equal(Kg, Ko) and np.array_equal(Vg, Vo)
     assert rapid.rapid_device_error(True) == 0
