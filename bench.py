@@ -456,6 +456,9 @@ def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
     e1.record(stream)
     torch.cuda.synchronize()
     eager_us = e0.elapsed_time(e1) / reps * 1e3
+    if n == 0:   # a single-query step has no speculative rows: the call launches nothing
+        return {"us_per_step": eager_us, "us_per_step_graph": None, "layers": w.layers,
+                "rows_moved_per_layer": 0, "bytes_moved": 0, "launches_per_step": 0}
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for _ in range(reps):
