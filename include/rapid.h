@@ -25,6 +25,9 @@
  *                      eta*(q - p)), the tail-preserving replacement of p_hat
  *                      by p where p_hat < 0.1 * max p_hat, and the adjusted
  *                      residual norm(max(p - p_hat, p - q))).
+ *                      rapid_accept_ex adds drafts of different lengths in
+ *                      one batch and a Philox key in device memory (CUDA-graph
+ *                      replays); rapid_accept_noalloc needs no workspace.
  *
  *   rapid_kv_commit    after acceptance, the accepted path's speculative K/V
  *   rapid_kv_advance   rows join the history next to the root, and the
@@ -53,6 +56,11 @@
  *    unspecified (but memory-safe) results.
  *  - No C++ exception crosses this ABI.  Calls are stateless and may be issued
  *    from several host threads on different streams.
+ *  - Every per-step quantity that changes between verify steps (history
+ *    lengths, paths, counts, and with rapid_accept_ex the Philox key)
+ *    is read from device memory, so one step can be captured in a CUDA graph
+ *    and replayed; make a call once outside the capture first (the first call
+ *    of a shape sets kernel attributes and looks up driver entry points).
  */
 #ifndef RAPID_H
 #define RAPID_H
@@ -195,6 +203,42 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft,
                           int32_t* n_accepted, int32_t* next_token, int32_t* path,
                           float* diag, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/*
+ * rapid_accept with two optional inputs in device memory: per-sequence node
+ * counts (drafts of different lengths in one batch) and the Philox key.
+ *
+ *  n_nodes          device int32 [B], 4-byte aligned, or NULL.  Sequence b has
+ *                   n_nodes[b] nodes, 1 <= n_nodes[b] <= n_q: node 0 (the
+ *                   root) and n_nodes[b] - 1 drafts, a chain or a tree as
+ *                   `parent` says.  n_accepted, next_token and path of sequence
+ *                   b are those of the same call on its first n_nodes[b] nodes
+ *                   alone: the nodes past the count are nobody's children and
+ *                   on no path, so a fully accepted short chain ends with the
+ *                   bonus draw from p of its last row.  The buffers keep the
+ *                   [B, n_q, ...] layout and the padding rows are still
+ *                   streamed, but their contents (any bits) affect no result;
+ *                   their diag entries are unspecified.  Counts outside
+ *                   [1, n_q] are clamped.  NULL: every sequence has n_q nodes.
+ *  philox_seed_dev  device address of one uint64_t, 8-byte aligned, or NULL.
+ *                   If given, the kernels read the key from there when they
+ *                   run (philox_seed is ignored), so a call captured once in a
+ *                   CUDA graph draws fresh numbers on every replay as long as
+ *                   the caller changes the value between replays (a kernel or
+ *                   a copy of its own inside the same graph).  The call does
+ *                   not write it.
+ *
+ * Every other argument, the results and the errors are those of rapid_accept;
+ * a misaligned n_nodes or philox_seed_dev returns RAPID_EINVAL.  With both
+ * NULL this is rapid_accept.
+ */
+rapid_status rapid_accept_ex(const float* z_target, const float* q_draft,
+                             const int32_t* draft_tokens, const int32_t* parent,
+                             const int32_t* n_nodes, int B, int n_q, int V, float T, float eta,
+                             uint64_t philox_seed, const uint64_t* philox_seed_dev,
+                             uint32_t flags, int32_t* n_accepted, int32_t* next_token,
+                             int32_t* path, float* diag, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /* Largest B * n_q that rapid_accept_noalloc accepts. */
 enum { RAPID_NOALLOC_MAX_NODES = 4096 };

@@ -101,6 +101,23 @@ struct RowsShared {
     int abort;                   // a wait gave up: stop waiting, let the kernel run out
 };
 
+// The Philox key of the call: the host's value, or the one in device memory
+// now (read through L2: an earlier kernel of the stream may have changed it;
+// both kernels read it only after griddep_wait()).
+__device__ __forceinline__ uint2 philox_key(const AcceptParams& p) {
+    if (!p.seed_dev) return make_uint2(p.seed_lo, p.seed_hi);
+    const unsigned long long s = __ldcg(p.seed_dev);
+    return make_uint2((uint32_t)(s & 0xffffffffull), (uint32_t)(s >> 32));
+}
+
+// Nodes of sequence b: n_q, or the caller's count clamped to [1, n_q].  The
+// nodes past it are padding: no one's children, never on a path.
+__device__ __forceinline__ int node_count(const AcceptParams& p, int b) {
+    if (!p.n_nodes) return p.n_q;
+    const int n = p.n_nodes[b];
+    return n < 1 ? 1 : (n > p.n_q ? p.n_q : n);
+}
+
 __device__ __forceinline__ int parent_of(const AcceptParams& p, int b, int i) {
     if (!p.parent) return i - 1;
     int par = p.parent[(int64_t)b * p.n_q + i];
@@ -335,9 +352,6 @@ accept_rows_kernel(const AcceptParams p) {
     }
     cluster.sync();   // barriers and padding in place before any copy or peer send
     griddep_wait();
-    // the selection kernel may be scheduled now: its CTAs cannot share an SM
-    // with this kernel's, so they take idle SMs and wait in griddep_wait()
-    // for this grid to finish, with their launch already behind them
 
     float* zb = bufs + (size_t)g * 2 * span;   // this group's row buffer
     float* qb = zb + span;
@@ -438,7 +452,8 @@ accept_rows_kernel(const AcceptParams p) {
         // uniform r_c of the ratio test, while the cluster reduces
         float r_c = 0.f;
         if (key >= 0) {
-            const Philox4 rnd = philox4x32_10((uint32_t)c, (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
+            const uint2 key = philox_key(p);
+            const Philox4 rnd = philox4x32_10((uint32_t)c, (uint32_t)b, 0u, 0u, key.x, key.y);
             r_c = word_uniform(rnd.w[0]);
         }
         wait_or_abort(&sh.mb1[g], (uint32_t)(k & 1), &sh.abort, p.err,
@@ -568,6 +583,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     const int warp = t >> 5, lane = t & 31;
     const int n_q = p.n_q;
     griddep_wait();
+    const int nn = node_count(p, b);   // nodes of this sequence
     if (t < n_q) {
         s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
         s_par[t] = t == 0 ? -1 : parent_of(p, b, t);
@@ -575,12 +591,12 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
         s_stats[t] = reinterpret_cast<const float4*>(p.ws_stats)[(int64_t)b * n_q + t];
     }
     __syncthreads();
-    if (t > 0 && t < n_q) s_kids[s_par[t]] = 1;   // every writer stores the same value
+    if (t > 0 && t < nn) s_kids[s_par[t]] = 1;   // every writer stores the same value
     __syncthreads();
 
     // every leaf: the number of accepted nodes from the root down its path
     int key = -1;
-    if (t < n_q) {
+    if (t < nn) {
         if (!s_kids[t]) {   // a leaf
             int depth = 0;
             for (int v = t; v != 0; v = s_par[v]) ++depth;
@@ -686,7 +702,8 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
         if (warp == 0) {   // the cluster's totals, in slice order
             const float mc = lane < p.C ? *cluster.map_shared_rank(&s_total[0], lane) : 0.f;
             const float totals = warp_sum(mc);
-            const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, p.seed_lo, p.seed_hi);
+            const uint2 key = philox_key(p);
+            const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, key.x, key.y);
             const float target = word_uniform(rnd.w[1]) * totals;
             float incl = mc;
 #pragma unroll

@@ -36,6 +36,12 @@ struct AcceptParams {
     int clamp;                   // tail rule on/off
     float invT, eta;
     uint32_t seed_lo, seed_hi;
+    // non-null: the key is read from here when the kernels run (seed_lo and
+    // seed_hi unused), so a call captured in a graph sees the current value
+    const unsigned long long* seed_dev;
+    // non-null: sequence b has n_nodes[b] nodes (clamped to [1, n_q]); the
+    // nodes past it take no part in the selection
+    const int32_t* n_nodes;
 };
 
 struct AcceptShape {

@@ -114,7 +114,8 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
 // rapid_lm_head_accept).
 rapid_status accept_launch(const float* z_target, const float* q_draft,
                            const int32_t* draft_tokens, const int32_t* parent, int B, int n_q,
-                           int V, float T, float eta, uint64_t philox_seed, uint32_t flags,
+                           const int32_t* n_nodes, int V, float T, float eta,
+                           uint64_t philox_seed, const uint64_t* philox_seed_dev, uint32_t flags,
                            int32_t* n_accepted, int32_t* next_token, int32_t* path, float* diag,
                            void* workspace, cudaStream_t st) {
     AcceptShape sh{};
@@ -137,6 +138,8 @@ rapid_status accept_launch(const float* z_target, const float* q_draft,
     p.eta = eta;
     p.seed_lo = (uint32_t)(philox_seed & 0xffffffffu);
     p.seed_hi = (uint32_t)(philox_seed >> 32);
+    p.seed_dev = reinterpret_cast<const unsigned long long*>(philox_seed_dev);
+    p.n_nodes = n_nodes;
     p.err = device_error_word();
     return launch_accept(p, sh, st) == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
 }
@@ -207,11 +210,12 @@ size_t rapid_accept_workspace_size(int B, int n_q, int V) {
     return align_up(rows * sizeof(int32_t)) + align_up(rows * 4 * sizeof(float));
 }
 
-rapid_status rapid_accept(const float* z_target, const float* q_draft, const int32_t* draft_tokens,
-                          const int32_t* parent, int B, int n_q, int V, float T, float eta,
-                          uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
-                          int32_t* next_token, int32_t* path, float* diag, void* workspace,
-                          size_t workspace_bytes, void* stream) {
+// Host checks shared by rapid_accept and rapid_accept_ex.
+static rapid_status accept_args(const float* z_target, const float* q_draft,
+                                const int32_t* draft_tokens, int B, int n_q, int V, float T,
+                                float eta, uint32_t flags, const int32_t* n_accepted,
+                                const int32_t* next_token, const void* workspace,
+                                size_t workspace_bytes) {
     if (!z_target || !q_draft || !draft_tokens || !n_accepted || !next_token || !workspace)
         return RAPID_EINVAL;
     if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return RAPID_EINVAL;
@@ -222,9 +226,38 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft, const int
     const size_t need = rapid_accept_workspace_size(B, n_q, V);
     if (workspace_bytes < need) return RAPID_ENOMEM;
     if (reinterpret_cast<uintptr_t>(workspace) & 15u) return RAPID_EINVAL;
-    return accept_launch(z_target, q_draft, draft_tokens, parent, B, n_q, V, T, eta, philox_seed,
-                         flags, n_accepted, next_token, path, diag, workspace,
-                         static_cast<cudaStream_t>(stream));
+    return RAPID_OK;
+}
+
+rapid_status rapid_accept(const float* z_target, const float* q_draft, const int32_t* draft_tokens,
+                          const int32_t* parent, int B, int n_q, int V, float T, float eta,
+                          uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
+                          int32_t* next_token, int32_t* path, float* diag, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+    const rapid_status s = accept_args(z_target, q_draft, draft_tokens, B, n_q, V, T, eta, flags,
+                                       n_accepted, next_token, workspace, workspace_bytes);
+    if (s != RAPID_OK) return s;
+    return accept_launch(z_target, q_draft, draft_tokens, parent, B, n_q, nullptr, V, T, eta,
+                         philox_seed, nullptr, flags, n_accepted, next_token, path, diag,
+                         workspace, static_cast<cudaStream_t>(stream));
+}
+
+rapid_status rapid_accept_ex(const float* z_target, const float* q_draft,
+                             const int32_t* draft_tokens, const int32_t* parent,
+                             const int32_t* n_nodes, int B, int n_q, int V, float T, float eta,
+                             uint64_t philox_seed, const uint64_t* philox_seed_dev,
+                             uint32_t flags, int32_t* n_accepted, int32_t* next_token,
+                             int32_t* path, float* diag, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (philox_seed_dev && (reinterpret_cast<uintptr_t>(philox_seed_dev) & 7u))
+        return RAPID_EINVAL;
+    if (n_nodes && (reinterpret_cast<uintptr_t>(n_nodes) & 3u)) return RAPID_EINVAL;
+    const rapid_status s = accept_args(z_target, q_draft, draft_tokens, B, n_q, V, T, eta, flags,
+                                       n_accepted, next_token, workspace, workspace_bytes);
+    if (s != RAPID_OK) return s;
+    return accept_launch(z_target, q_draft, draft_tokens, parent, B, n_q, n_nodes, V, T, eta,
+                         philox_seed, philox_seed_dev, flags, n_accepted, next_token, path, diag,
+                         workspace, static_cast<cudaStream_t>(stream));
 }
 
 rapid_status rapid_lm_head(const void* hidden, const void* W_lm, int rows, int hidden_dim, int V,
@@ -272,8 +305,8 @@ rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidd
     if (launch_lm_head(hidden, W_lm, B * n_q, hidden_dim, V, z, device_error_word(), st) !=
         cudaSuccess)
         return RAPID_ECUDA;
-    return accept_launch(z, q_draft, draft_tokens, parent, B, n_q, V, T, eta, philox_seed, flags,
-                         n_accepted, next_token, path, diag, acc_ws, st);
+    return accept_launch(z, q_draft, draft_tokens, parent, B, n_q, nullptr, V, T, eta, philox_seed,
+                         nullptr, flags, n_accepted, next_token, path, diag, acc_ws, st);
 }
 
 const char* rapid_status_string(int status) {

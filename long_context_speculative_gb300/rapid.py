@@ -16,6 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librapid.so")
 
 RAPID_OK = 0
+RAPID_EINVAL = -1
 RAPID_DTYPE_F32 = 0
 RAPID_DTYPE_BF16 = 1
 RAPID_ACCEPT_TAIL_CLAMP = 1
@@ -54,6 +55,9 @@ def lib() -> ctypes.CDLL:
     L.rapid_accept.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp, vp, vp,
                                vp, sz, vp]
     L.rapid_accept.restype = i32
+    L.rapid_accept_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, vp, u32, vp,
+                                  vp, vp, vp, vp, sz, vp]
+    L.rapid_accept_ex.restype = i32
     L.rapid_status_string.argtypes = [i32]
     L.rapid_status_string.restype = ctypes.c_char_p
     L.rapid_version.argtypes = []
@@ -151,6 +155,31 @@ def rapid_accept(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, f
                             _ptr(diag), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "rapid_accept")
+
+
+def rapid_accept_ex(z_target, q_draft, draft_tokens, parent, n_nodes, T, eta, philox_seed,
+                    flags, n_accepted, next_token, path, diag, workspace, stream=None):
+    """rapid_accept with optional per-sequence node counts n_nodes (int32 [B] CUDA tensor or
+    None) and a Philox key that is either an int or a one-element 64-bit integer CUDA tensor
+    read by the kernels when they run."""
+    _need_cuda(z_target, q_draft, draft_tokens, parent, n_nodes, n_accepted, next_token, path,
+               diag, workspace)
+    B, n_q, V = z_target.shape
+    if n_nodes is not None and (n_nodes.dtype != torch.int32 or n_nodes.numel() != B):
+        raise RapidError("n_nodes must be an int32 tensor of B entries")
+    if isinstance(philox_seed, torch.Tensor):
+        _need_cuda(philox_seed)
+        if philox_seed.dtype not in (torch.int64, torch.uint64) or philox_seed.numel() != 1:
+            raise RapidError("a device philox_seed must be a one-element 64-bit integer tensor")
+        key, key_dev = 0, _ptr(philox_seed)
+    else:
+        key, key_dev = int(philox_seed) & ((1 << 64) - 1), None
+    st = lib().rapid_accept_ex(_ptr(z_target), _ptr(q_draft), _ptr(draft_tokens), _ptr(parent),
+                               _ptr(n_nodes), B, n_q, V, float(T), float(eta), key, key_dev,
+                               int(flags), _ptr(n_accepted), _ptr(next_token), _ptr(path),
+                               _ptr(diag), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "rapid_accept_ex")
 
 
 def rapid_accept_noalloc(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, flags,
@@ -302,8 +331,12 @@ def verify_attn(Q, K, V, prefix_len, spec_mask=None, softmax_scale=0.0, out=None
 
 
 def accept(z, q, tokens, parent=None, T=1.0, eta=1.0, seed=0, tail_clamp=True, want_path=True,
-           want_diag=True, workspace=None, stream=None):
-    """Dict of device tensors n_accepted [B], next_token [B], path [B,n_q], diag [B,n_q,5]."""
+           want_diag=True, workspace=None, stream=None, n_nodes=None):
+    """Dict of device tensors n_accepted [B], next_token [B], path [B,n_q], diag [B,n_q,5].
+
+    seed: the Philox key as an int, or a one-element int64 CUDA tensor that the kernels read
+    when they run.  n_nodes: None, or int32 [B] node counts of drafts shorter than n_q.
+    Either one goes through rapid_accept_ex."""
     B, n_q, V = z.shape
     dev = z.device
     n_acc = torch.empty(B, dtype=torch.int32, device=dev)
@@ -316,8 +349,12 @@ def accept(z, q, tokens, parent=None, T=1.0, eta=1.0, seed=0, tail_clamp=True, w
             raise RapidError("unsupported accept shape")
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     flags = RAPID_ACCEPT_TAIL_CLAMP if tail_clamp else 0
-    rapid_accept(z, q, tokens, parent, T, eta, seed, flags, n_acc, nxt, path, diag, workspace,
-                 stream)
+    if isinstance(seed, torch.Tensor) or n_nodes is not None:
+        rapid_accept_ex(z, q, tokens, parent, n_nodes, T, eta, seed, flags, n_acc, nxt, path,
+                        diag, workspace, stream)
+    else:
+        rapid_accept(z, q, tokens, parent, T, eta, seed, flags, n_acc, nxt, path, diag,
+                     workspace, stream)
     return dict(n_accepted=n_acc, next_token=nxt, path=path, diag=diag)
 
 

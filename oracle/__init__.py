@@ -69,7 +69,8 @@ def lib():
         L.orc_kd_grad.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_double, _dp]
         L.orc_distilled_logits.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, _dp]
-        L.orc_accept.argtypes = [_fp, _fp, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        L.orc_accept.argtypes = [_fp, _fp, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_int,
                                  ctypes.c_double, ctypes.c_double, ctypes.c_uint64, ctypes.c_int,
                                  _i32p, _i32p, _i32p, _dp, _dp, ctypes.c_int]
         L.orc_kv_commit.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -241,8 +242,12 @@ def distilled_logits(z, q, T, eta):
     return out
 
 
-def accept(z, q, tokens, parent=None, T=1.0, eta=0.0, seed=0, clamp=True, nthreads=None):
+def accept(z, q, tokens, parent=None, T=1.0, eta=0.0, seed=0, clamp=True, nthreads=None,
+           n_nodes=None):
     """Whole acceptance step.  z, q [B, n_q, V] float32; tokens/parent [B, n_q] int32.
+
+    n_nodes: None, or [B] node counts in [1, n_q]; sequence b is then the same
+    step on its first n_nodes[b] nodes (diag zero past them).
 
     Returns dict(n_accepted [B], next_token [B], path [B,n_q], diag [B,n_q,5],
     sample [B,6] = (row e, kind, u, W, u*W, token)).
@@ -252,13 +257,18 @@ def accept(z, q, tokens, parent=None, T=1.0, eta=0.0, seed=0, clamp=True, nthrea
     B, n_q, V = z.shape
     tok = _c(tokens, np.int32)
     par = None if parent is None else _c(parent, np.int32)
+    nn = None
+    if n_nodes is not None:
+        nn = _c(n_nodes, np.int32)
+        assert nn.shape == (B,) and (nn >= 1).all() and (nn <= n_q).all()
     n_acc = np.zeros(B, np.int32)
     nxt = np.zeros(B, np.int32)
     path = np.zeros((B, n_q), np.int32)
     diag = np.zeros((B, n_q, 5), np.float64)
     info = np.zeros((B, 6), np.float64)
     lib().orc_accept(_ptr(z, _fp), _ptr(q, _fp), _ptr(tok, _i32p),
-                     None if par is None else _ptr(par, _i32p), B, n_q, V, float(T), float(eta),
+                     None if par is None else _ptr(par, _i32p),
+                     None if nn is None else _ptr(nn, _i32p), B, n_q, V, float(T), float(eta),
                      int(seed), int(bool(clamp)), _ptr(n_acc, _i32p), _ptr(nxt, _i32p),
                      _ptr(path, _i32p), _ptr(diag, _dp), _ptr(info, _dp),
                      nthreads or default_threads())

@@ -334,6 +334,7 @@ struct AcceptProblem {
     const float* q;
     const int32_t* tokens;
     const int32_t* parent;  // NULL: chain
+    const int32_t* n_nodes; // NULL: n_q nodes in every sequence
     int B, n_q, V;
     double T, eta;
     uint64_t seed;
@@ -344,16 +345,21 @@ int parent_of(const AcceptProblem& A, int b, int i) {
     return A.parent ? A.parent[(int64_t)b * A.n_q + i] : i - 1;
 }
 
+// A sequence with n nodes (a draft shorter than the batch's n_q) is the same
+// step on its first n nodes alone: only the strides of the [B, n_q, ...]
+// arrays still use n_q.  The nodes past n are not looked at.
 void accept_one(const AcceptProblem& A, int b, int32_t* n_acc, int32_t* next_tok, int32_t* path,
                 double* diag, double* sample_info) {
-    const int n_q = A.n_q, V = A.V;
+    const int stride = A.n_q, V = A.V;
+    const int n_q = A.n_nodes ? A.n_nodes[b] : A.n_q;   // nodes of this sequence
     const int64_t rowsz = V;
     std::vector<std::vector<double>> P(n_q), PH(n_q);
     std::vector<double> scratch(V);
+    if (diag) for (int c = 0; c < stride * 5; ++c) diag[(int64_t)b * stride * 5 + c] = 0.0;
     for (int j = 0; j < n_q; ++j) {
         P[j].resize(V);
         PH[j].resize(V);
-        const int64_t off = ((int64_t)b * n_q + j) * rowsz;
+        const int64_t off = ((int64_t)b * stride + j) * rowsz;
         row_dists(A.z + off, A.q + off, V, A.T, A.eta, A.clamp, P[j].data(), scratch.data(),
                   PH[j].data());
     }
@@ -362,20 +368,19 @@ void accept_one(const AcceptProblem& A, int b, int32_t* n_acc, int32_t* next_tok
     std::vector<int> accepted(n_q, 0);
     for (int i = 1; i < n_q; ++i) {
         const int j = parent_of(A, b, i);
-        const int t = A.tokens[(int64_t)b * n_q + i];
+        const int t = A.tokens[(int64_t)b * stride + i];
         const double pt = P[j][t];
         const double ph = PH[j][t];
-        const double qt = (double)A.q[((int64_t)b * n_q + j) * rowsz + t];
+        const double qt = (double)A.q[((int64_t)b * stride + j) * rowsz + t];
         const double ratio = (qt == 0.0) ? std::numeric_limits<double>::infinity() : ph / qt;
         double r;
         node_uniforms(A.seed, b, i, &r, nullptr);
         accepted[i] = (r <= std::min(1.0, ratio)) ? 1 : 0;
         if (diag) {
-            double* dg = diag + ((int64_t)b * n_q + i) * 5;
+            double* dg = diag + ((int64_t)b * stride + i) * 5;
             dg[0] = pt; dg[1] = ph; dg[2] = qt; dg[3] = ratio; dg[4] = r;
         }
     }
-    if (diag) for (int c = 0; c < 5; ++c) diag[(int64_t)b * n_q * 5 + c] = 0.0;
 
     // Children lists; leaves are nodes without children.
     std::vector<int> n_children(n_q, 0);
@@ -408,7 +413,7 @@ void accept_one(const AcceptProblem& A, int b, int32_t* n_acc, int32_t* next_tok
     std::vector<double> w(V);
     int kind;
     if (n_children[e] > 0) {
-        const int64_t off = ((int64_t)b * n_q + e) * rowsz;
+        const int64_t off = ((int64_t)b * stride + e) * rowsz;
         residual_weights(P[e].data(), PH[e].data(), A.q + off, V, w.data());
         double W = 0.0;
         for (int k = 0; k < V; ++k) W += w[k];
@@ -427,7 +432,7 @@ void accept_one(const AcceptProblem& A, int b, int32_t* n_acc, int32_t* next_tok
     n_acc[b] = best_len;
     next_tok[b] = tok;
     if (path) {
-        for (int n = 0; n < n_q; ++n) path[(int64_t)b * n_q + n] = n < best_len ? best_nodes[n] : -1;
+        for (int n = 0; n < stride; ++n) path[(int64_t)b * stride + n] = n < best_len ? best_nodes[n] : -1;
     }
     if (sample_info) {
         double* si = sample_info + (int64_t)b * 6;
@@ -670,10 +675,10 @@ void orc_distilled_logits(const double* z, const double* q, int V, double T, dou
 // kind 0=bonus/1=residual/2=residual fell back to p, u, W, u*W, token) are
 // optional.
 void orc_accept(const float* z, const float* q, const int32_t* tokens, const int32_t* parent,
-                int B, int n_q, int V, double T, double eta, uint64_t seed, int clamp,
-                int32_t* n_acc, int32_t* next_tok, int32_t* path, double* diag,
-                double* sample_info, int nthreads) {
-    AcceptProblem A{z, q, tokens, parent, B, n_q, V, T, eta, seed, clamp};
+                const int32_t* n_nodes, int B, int n_q, int V, double T, double eta,
+                uint64_t seed, int clamp, int32_t* n_acc, int32_t* next_tok, int32_t* path,
+                double* diag, double* sample_info, int nthreads) {
+    AcceptProblem A{z, q, tokens, parent, n_nodes, B, n_q, V, T, eta, seed, clamp};
     parallel_for(B, nthreads, [&](int64_t b) {
         accept_one(A, (int)b, n_acc, next_tok, path, diag, sample_info);
     });

@@ -38,7 +38,7 @@ def _parents(par, b, n_q):
 
 
 def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref, prob_rtol=PROB_RTOL,
-                 exempt=EXEMPT):
+                 exempt=EXEMPT, n_nodes=None):
     """Compare one rapid_accept call with oracle.accept on the same inputs.
 
     gpu: dict of numpy arrays (n_accepted, next_token, path, diag) from the CUDA path.
@@ -46,6 +46,9 @@ def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref, prob_rtol=PRO
     prob_rtol / exempt widen the probability tolerance and the near-boundary
     bands when the GPU's logits themselves carry an error (the fused LM-head
     path): a softmax moves by at most 2 max|dz| / T in relative terms.
+    n_nodes: per-sequence node counts of a ragged batch; the nodes past them
+    are padding and only the real ones are compared (their diag entries are
+    unspecified on the GPU).
     """
     EXEMPT = exempt
     B, n_q, V = z.shape
@@ -54,7 +57,8 @@ def check_accept(z, q, tokens, par, T, eta, seed, clamp, gpu, ref, prob_rtol=PRO
         parents = _parents(par, b, n_q)
         dg, dr = gpu["diag"][b], ref["diag"][b]
         exempt_nodes = set()
-        for i in range(1, n_q):
+        nn = n_q if n_nodes is None else int(n_nodes[b])
+        for i in range(1, nn):
             j = parents[i]
             t = int(tokens[b, i])
             # clamp-threshold exemption: p_hat(t) within 1e-5 of 0.1 max p_hat

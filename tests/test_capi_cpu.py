@@ -48,6 +48,15 @@ def test_host_validation_without_gpu(lib):
                                  None, None, 0, None) == -1
     assert lib.rapid_accept(None, None, None, None, 1, 3, 100, 1.0, 1.0, 0, 1, None, None, None,
                             None, None, 0, None) == -1
+    # rapid_accept_ex: misaligned node counts or key address, NULL tensors, bad sizes
+    fake = ctypes.c_void_p(256)   # an aligned fake device address (never dereferenced)
+    for nn, key in ((ctypes.c_void_p(258), None), (None, ctypes.c_void_p(260))):
+        assert lib.rapid_accept_ex(fake, fake, fake, None, nn, 1, 3, 100, 1.0, 1.0, 0, key, 1,
+                                   fake, fake, None, None, fake, 1 << 20, None) == -1
+    assert lib.rapid_accept_ex(None, None, None, None, None, 1, 3, 100, 1.0, 1.0, 0, fake, 1,
+                               None, None, None, None, None, 0, None) == -1
+    assert lib.rapid_accept_ex(fake, fake, fake, None, fake, 1, 65, 100, 1.0, 1.0, 0, None, 1,
+                               fake, fake, None, None, fake, 1 << 20, None) == -1
     # Sizes outside the supported range report a zero workspace.
     assert lib.rapid_verify_attn_workspace_size(1, 4, 1, 96, 5, 64, 1) == 0
     assert lib.rapid_verify_attn_workspace_size(1, 4, 1, 128, 65, 640, 1) == 0

@@ -132,3 +132,65 @@ def test_c_abi_rejects_bad_arguments():
         bad = list(args)
         bad[idx] = val
         assert L.rapid_accept(*bad) == code, (idx, val)
+
+
+def _garbage_padding(z, q, tok, n_nodes, seed):
+    """Rows and tokens past each sequence's node count: NaN / inf logits, NaN
+    probabilities and token ids outside the vocabulary (negative and huge)."""
+    g = torch.Generator().manual_seed(seed)
+    z, q, tok = z.clone(), q.clone(), tok.clone()
+    for b, n in enumerate(n_nodes):
+        pick = torch.rand(z[b, n:].shape, generator=g) < 0.5
+        z[b, n:] = torch.where(pick, torch.tensor(float("nan")), torch.tensor(float("inf")))
+        q[b, n:] = float("nan")
+        tok[b, n:] = torch.where(torch.rand(tok[b, n:].shape, generator=g) < 0.5,
+                                 torch.tensor(-7, dtype=torch.int32),
+                                 torch.tensor(1 << 30, dtype=torch.int32))
+    return z, q, tok
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_ragged_drafts_through_rapid_accept_ex(tree):
+    # drafts of different lengths in one batch: the CUDA path with node counts
+    # against the oracle with the same counts, padding full of garbage
+    if tree:
+        w = wl.QWEN7B_TREE
+        n_nodes = np.array([32, 1, 17, 9], np.int32)
+    else:
+        w = wl.LLAMA8B_LAYER_32K
+        n_nodes = np.array([11, 1, 5, 2, 11, 8], np.int32)
+    inp = wl.accept_inputs(w, T=1.0, B=len(n_nodes))
+    z, q, tok = _garbage_padding(inp.z, inp.q, inp.tokens, n_nodes, seed=3)
+    par = inp.parent
+    nn_d = torch.from_numpy(n_nodes).to(DEV)
+    seen_bonus = 0
+    for seed in (11, 12, 13):
+        res = rapid.accept(z.to(DEV), q.to(DEV), tok.to(DEV),
+                           None if par is None else par.to(DEV), T=1.0, eta=1.0, seed=seed,
+                           n_nodes=nn_d)
+        torch.cuda.synchronize()
+        gpu = {k: v.cpu().numpy() for k, v in res.items()}
+        zn, qn, tn = z.numpy(), q.numpy(), tok.numpy()
+        pn = None if par is None else par.numpy()
+        ref = oracle.accept(zn, qn, tn, pn, T=1.0, eta=1.0, seed=seed, n_nodes=n_nodes)
+        stats = check_accept(zn, qn, tn, pn, 1.0, 1.0, seed, True, gpu, ref, n_nodes=n_nodes)
+        assert stats["compared"] >= len(n_nodes) - 1
+        seen_bonus += int((ref["sample"][:, 1] == 0).sum())
+        # a single-node sequence draws its next token from p of the root row
+        one = np.nonzero(n_nodes == 1)[0]
+        assert (gpu["n_accepted"][one] == 0).all() and (gpu["path"][one] == -1).all()
+    assert seen_bonus >= 3   # the single-node sequences at least
+    assert rapid.rapid_device_error(True) == 0
+
+
+def test_ragged_full_counts_equal_rapid_accept():
+    # node counts of n_q everywhere give rapid_accept's results bit for bit
+    w = wl.LLAMA8B_LAYER_32K
+    inp = wl.accept_inputs(w, T=1.0, B=3)
+    z, q, tok = inp.z.to(DEV), inp.q.to(DEV), inp.tokens.to(DEV)
+    full = torch.full((3,), w.n_q, dtype=torch.int32, device=DEV)
+    a = rapid.accept(z, q, tok, None, T=1.0, eta=1.0, seed=21)
+    b = rapid.accept(z, q, tok, None, T=1.0, eta=1.0, seed=21, n_nodes=full)
+    torch.cuda.synchronize()
+    for k in ("n_accepted", "next_token", "path", "diag"):
+        assert torch.equal(a[k], b[k]), k

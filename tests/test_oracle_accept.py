@@ -316,3 +316,69 @@ def test_single_query_row_is_bonus_draw():
         c = np.cumsum(p)
         expect = int(np.argmax(c > u * c[-1]))
         assert res["n_accepted"][0] == 0 and res["next_token"][0] == expect
+
+
+def _garbage_padding(z, q, tok, n_nodes, rng):
+    """Rows and tokens past each sequence's node count filled with values that
+    would change any result they entered (NaN / inf logits, NaN
+    probabilities, a token id far outside the vocabulary)."""
+    z, q, tok = z.copy(), q.copy(), tok.copy()
+    for b, n in enumerate(n_nodes):
+        z[b, n:] = np.where(rng.random(z[b, n:].shape) < 0.5, np.nan, np.inf)
+        q[b, n:] = np.nan
+        tok[b, n:] = 1 << 30
+    return z, q, tok
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_ragged_drafts_equal_truncated_batches(tree):
+    # Sequence b with n_nodes[b] nodes is the step on its first n_nodes[b]
+    # nodes: for every count m, the sequences with m nodes give what a batch
+    # with n_q = m gives (same sequence index b, so the same Philox blocks),
+    # whatever sits in the padding.
+    B, n_q = 6, 10
+    w = wl.Workload("ragged", B=B, Hq=1, Hkv=1, d=64, n_q=n_q, prefix=1, layers=1, V=400,
+                    dtype="f32", z_std=2.0, q_noise_std=1.0, q_noise_uses_T=True, tree=tree,
+                    tree_nodes_max_depth=4, seed=51 if tree else 50)
+    inp = wl.accept_inputs(w)
+    z, q, tok = inp.z.numpy(), inp.q.numpy(), inp.tokens.numpy()
+    par = None if inp.parent is None else inp.parent.numpy()
+    n_nodes = np.array([4, n_q, 1, 4, 7, 2], np.int32)
+    rng = np.random.default_rng(5)
+    zg, qg, tg = _garbage_padding(z, q, tok, n_nodes, rng)
+    for seed in range(12):
+        res = oracle.accept(zg, qg, tg, par, T=1.0, eta=1.0, seed=seed, n_nodes=n_nodes)
+        for m in sorted(set(n_nodes.tolist())):
+            ref = oracle.accept(z[:, :m], q[:, :m], tok[:, :m],
+                                None if par is None else par[:, :m], T=1.0, eta=1.0, seed=seed)
+            for b in np.nonzero(n_nodes == m)[0]:
+                assert res["n_accepted"][b] == ref["n_accepted"][b]
+                assert res["next_token"][b] == ref["next_token"][b]
+                np.testing.assert_array_equal(res["path"][b, :m], ref["path"][b])
+                assert (res["path"][b, m:] == -1).all()
+                np.testing.assert_array_equal(res["diag"][b, :m], ref["diag"][b])
+                assert (res["diag"][b, m:] == 0).all()
+                np.testing.assert_array_equal(res["sample"][b], ref["sample"][b])
+
+
+def test_ragged_fully_accepted_chain_ends_with_bonus_from_its_last_row():
+    # q = p (eta = 0): every ratio is 1 and every draft is accepted, so a
+    # chain of m nodes accepts m - 1 drafts and draws the bonus token from p of
+    # row m - 1 with u_m, by inverse CDF (computed here with numpy).
+    B, n_q, V, T = 4, 9, 60, 0.8
+    rng = np.random.default_rng(12)
+    z = (rng.standard_normal((B, n_q, V)) * 2).astype(np.float32)
+    q = sp_softmax(z.astype(np.float64) / T, axis=-1).astype(np.float32)
+    tok = rng.integers(0, V, size=(B, n_q)).astype(np.int32)
+    n_nodes = np.array([3, 9, 1, 6], np.int32)
+    zg, qg, tg = _garbage_padding(z, q, tok, n_nodes, rng)
+    for seed in range(8):
+        res = oracle.accept(zg, qg, tg, None, T=T, eta=0.0, seed=seed, n_nodes=n_nodes)
+        for b, m in enumerate(n_nodes):
+            assert res["n_accepted"][b] == m - 1
+            assert list(res["path"][b][:m - 1]) == list(range(1, m))
+            assert int(res["sample"][b, 0]) == m - 1 and int(res["sample"][b, 1]) == 0
+            p = sp_softmax(z[b, m - 1].astype(np.float64) / T)
+            _, u = oracle.node_uniforms(seed, b, m)
+            c = np.cumsum(p)
+            assert res["next_token"][b] == int(np.argmax(c > u * c[-1]))
