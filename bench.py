@@ -362,6 +362,8 @@ def run_gpu(args, w):
     acc_tree = None
     if not w.tree:
         acc_tree = accept_batch_roofline(wl.QWEN7B_TREE, dev, stream, B=wl.QWEN7B_TREE.B)
+    # and on the same batch with drafts of different lengths (padding rows skipped)
+    acc_ragged = accept_batch_roofline(w, dev, stream, ragged=True)
 
     # ---- KV commit of an accepted path, all layers (moves the cache rows last) -
     kv_commit = kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream)
@@ -406,6 +408,7 @@ def run_gpu(args, w):
                     "d2h_bytes_per_step": d2h},
             "accept_roofline": acc_roof,
             "accept_roofline_tree": acc_tree,
+            "accept_ragged": acc_ragged,
             "kv_commit": kv_commit,
             "retrieval": retrieval,
             "lm_head_accept": lm_head,
@@ -606,12 +609,13 @@ def retrieval_timing(w, dev, stream, D=1024, reps=20):
     return out
 
 
-def accept_batch_roofline(w, dev, stream, reps=20, B=None):
+def accept_batch_roofline(w, dev, stream, reps=20, B=None, ragged=False):
     """rapid_accept alone on a batch of at least 100 MB of z + q (larger than L2):
     the workload's own batch when that is large enough (the 4-sequence tree of
     the Qwen shape: 155.7 MB), else 16 sequences of its rows, more if that stays
     under 100 MB.  Algorithmic bytes = 8 B per vocabulary entry (z and q read
-    once) / CUDA-event time per call."""
+    once) / CUDA-event time per call.  ragged: the same batch with seeded draft
+    lengths 1..n_q per sequence (rapid_accept_ex); only the real rows count."""
     import torch
 
     from long_context_speculative_gb300 import rapid
@@ -627,27 +631,45 @@ def accept_batch_roofline(w, dev, stream, reps=20, B=None):
     z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
     par = None if inp.parent is None else inp.parent.to(dev)
     nbytes = z.numel() * 4 + q.numel() * 4
+    nn = None
+    if ragged:
+        g = torch.Generator().manual_seed(w.seed + 404)
+        counts = torch.randint(1, w.n_q + 1, (Bb,), generator=g, dtype=torch.int32)
+        nn = counts.to(dev)
+        nbytes = int(counts.sum()) * w.V * 8
     ws = torch.empty(rapid.rapid_accept_workspace_size(Bb, w.n_q, w.V), dtype=torch.uint8,
                      device=dev)
     na = torch.empty(Bb, dtype=torch.int32, device=dev)
     nt = torch.empty(Bb, dtype=torch.int32, device=dev)
+
+    def call(seed):
+        if nn is None:
+            rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                               na, nt, None, None, ws)
+        else:
+            rapid.rapid_accept_ex(z, q, tok, par, nn, w.T, w.eta, seed,
+                                  rapid.RAPID_ACCEPT_TAIL_CLAMP, na, nt, None, None, ws)
+
     for i in range(3):
-        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, i, rapid.RAPID_ACCEPT_TAIL_CLAMP, na, nt,
-                           None, None, ws)
+        call(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(reps):
-        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, 100 + i, rapid.RAPID_ACCEPT_TAIL_CLAMP,
-                           na, nt, None, None, ws)
+        call(100 + i)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     achieved = nbytes / (ms * 1e-3) / 1e9
     peak, src = _peaks()
+    if nn is None:
+        batch = f"{Bb} x {w.n_q} x {w.V} fp32 z and q ({nbytes / 1e6:.1f} MB, > L2)"
+    else:
+        batch = (f"{Bb} x {w.n_q} x {w.V} fp32 z and q, draft lengths 1..{w.n_q} "
+                 f"({int(counts.sum())} real rows: {nbytes / 1e6:.1f} MB)")
     return {"bound": "hbm", "kernel": "rapid_accept (row + select kernels)",
-            "batch": f"{Bb} x {w.n_q} x {w.V} fp32 z and q ({nbytes / 1e6:.1f} MB, > L2)",
+            "batch": batch,
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "avg_launch_ms": ms, "peak_source": src + " (hbm_gbs, copy)"}
 

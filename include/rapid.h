@@ -216,9 +216,10 @@ rapid_status rapid_accept(const float* z_target, const float* q_draft,
  *                   alone: the nodes past the count are nobody's children and
  *                   on no path, so a fully accepted short chain ends with the
  *                   bonus draw from p of its last row.  The buffers keep the
- *                   [B, n_q, ...] layout and the padding rows are still
- *                   streamed, but their contents (any bits) affect no result;
- *                   their diag entries are unspecified.  Counts outside
+ *                   [B, n_q, ...] layout; the padding rows of z_target and
+ *                   q_draft are not read, the padding tokens and parents
+ *                   (any values) affect no result, and the padding diag
+ *                   entries are unspecified.  Counts outside
  *                   [1, n_q] are clamped.  NULL: every sequence has n_q nodes.
  *  philox_seed_dev  device address of one uint64_t, 8-byte aligned, or NULL.
  *                   If given, the kernels read the key from there when they

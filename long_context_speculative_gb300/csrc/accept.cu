@@ -356,7 +356,19 @@ accept_rows_kernel(const AcceptParams p) {
     float* zb = bufs + (size_t)g * 2 * span;   // this group's row buffer
     float* qb = zb + span;
     auto row_of = [&](int i) -> int64_t { return cid + (int64_t)i * p.nclusters; };
+    // A row of a node past its sequence's node count is padding: every CTA of
+    // the cluster skips it alike (no copy, no exchange, no result).
+    auto padding = [&](int i) -> bool {
+        if (!p.n_nodes) return false;
+        const int64_t row = row_of(i);
+        const int b = (int)(row / p.n_q);
+        return (int)(row - (int64_t)b * p.n_q) >= node_count(p, b);
+    };
     auto load_row = [&](int i) {      // one thread, bulk path
+        if (padding(i)) {             // completes the buffer's phase with nothing to land
+            mbar_arrive(&sh.full[g]);
+            return;
+        }
         mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 8));
         if (n > 0) {
             const int64_t off = row_of(i) * p.V + lo;
@@ -367,7 +379,7 @@ accept_rows_kernel(const AcceptParams p) {
     // L2 prefetch of a later row of this group, so that its bulk copy, issued
     // only once the buffer is free, is served from L2
     auto prefetch_row = [&](int i) {   // one thread, bulk path
-        if (i < nrows && n > 0) {
+        if (i < nrows && n > 0 && !padding(i)) {
             const int64_t off = row_of(i) * p.V + lo;
             bulk_prefetch_l2(p.z + off, (uint32_t)(n * 4));
             bulk_prefetch_l2(p.q + off, (uint32_t)(n * 4));
@@ -395,13 +407,30 @@ accept_rows_kernel(const AcceptParams p) {
     // independently; the last warp of a phase combines the group's partials
     // and sends them to the cluster, and every warp waits for the cluster's
     // partials itself.  The other group computes while this one waits.
+    // Row i of the cluster's list is the group's (i >> 1)-th row: the phase of
+    // full[g].  kx counts the rows the group has exchanged (padding rows are
+    // not): the phase of mb1[g] and mb2[g].
+    int kx = 0;
 #pragma unroll 1
-    for (int k = 0;; ++k) {
-        const int i = 2 * k + g;
-        if (i >= nrows) break;
+    for (int i = g; i < nrows; i += 2) {
         const int64_t row = row_of(i);
         const int b = (int)(row / p.n_q);
         const int j = (int)(row - (int64_t)b * p.n_q);
+        if (padding(i)) {
+            // The buffer's phase for this row completed without a copy.  The
+            // group's warps last read the buffer in pass 2 of an earlier row,
+            // and thread 0 got here only after that row's reduction 2, which
+            // needs every warp's pass 2: the next row may take the buffer now.
+            prefetch_node(i + 2);
+            if (tg == 0) {
+                if (i == 0) mbar_arrive(&sh.stagger);
+                if (p.bulk && i + 2 < nrows) {
+                    fence_proxy_async_smem();
+                    load_row(i + 2);
+                }
+            }
+            continue;
+        }
         if (tg == 0) {
             // arm this row's exchange barriers (their previous phases completed
             // before any warp of the group could finish the previous row)
@@ -413,10 +442,10 @@ accept_rows_kernel(const AcceptParams p) {
         prefetch_node(i + 2);
         // the groups run half a row apart, so that one computes while the
         // other waits on the cluster
-        if (g == 1 && k == 0)
+        if (i == 1)
             wait_or_abort(&sh.stagger, 0u, &sh.abort, p.err, 0x06000000u);
         if (p.bulk) {
-            wait_or_abort(&sh.full[g], (uint32_t)(k & 1), &sh.abort, p.err,
+            wait_or_abort(&sh.full[g], (uint32_t)((i >> 1) & 1), &sh.abort, p.err,
                           0x01000000u | (unsigned)(i & 0xffff));
         } else {
             const int64_t off = row * p.V + lo;
@@ -456,7 +485,7 @@ accept_rows_kernel(const AcceptParams p) {
             const Philox4 rnd = philox4x32_10((uint32_t)c, (uint32_t)b, 0u, 0u, key.x, key.y);
             r_c = word_uniform(rnd.w[0]);
         }
-        wait_or_abort(&sh.mb1[g], (uint32_t)(k & 1), &sh.abort, p.err,
+        wait_or_abort(&sh.mb1[g], (uint32_t)(kx & 1), &sh.abort, p.err,
                       0x03000000u | (unsigned)(i & 0xffff));
         {
             MS r1{-INFINITY, 0.f};
@@ -465,7 +494,7 @@ accept_rows_kernel(const AcceptParams p) {
             st.m1 = r1.m;
             st.s1 = r1.s;
         }
-        if (g == 0 && k == 0 && tg == 0) mbar_arrive(&sh.stagger);
+        if (i == 0 && tg == 0) mbar_arrive(&sh.stagger);
         // pass 2; the group's last warp sends the slice's (reference, s, max a)
         {
             float amw;
@@ -491,8 +520,9 @@ accept_rows_kernel(const AcceptParams p) {
                 }
             }
         }
-        wait_or_abort(&sh.mb2[g], (uint32_t)(k & 1), &sh.abort, p.err,
+        wait_or_abort(&sh.mb2[g], (uint32_t)(kx & 1), &sh.abort, p.err,
                       0x02000000u | (unsigned)(i & 0xffff));
+        ++kx;
         float m2, s2;
         {
             MS r2{-INFINITY, 0.f};
