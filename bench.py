@@ -368,6 +368,8 @@ def run_gpu(args, w):
         acc_tree = accept_batch_roofline(wl.QWEN7B_TREE, dev, stream, B=wl.QWEN7B_TREE.B)
     # and on the same batch with drafts of different lengths (padding rows skipped)
     acc_ragged = accept_batch_roofline(w, dev, stream, ragged=True)
+    # and on a batch large enough to amortise the per-call latency (128 sequences)
+    acc_large = accept_batch_roofline(w, dev, stream, B=128)
 
     # ---- KV commit of an accepted path, all layers (moves the cache rows last) -
     kv_commit = kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream)
@@ -419,6 +421,7 @@ def run_gpu(args, w):
             "accept_roofline": acc_roof,
             "accept_roofline_tree": acc_tree,
             "accept_ragged": acc_ragged,
+            "accept_roofline_large": acc_large,
             "kv_commit": kv_commit,
             "retrieval": retrieval,
             "lm_head_accept": lm_head,
@@ -619,6 +622,37 @@ def retrieval_timing(w, dev, stream, D=1024, reps=20):
     return out
 
 
+def _device_accept_inputs(w, B, dev):
+    """The acceptance inputs of workloads.accept_inputs (z ~ N(0, z_std^2),
+    q = softmax(z/T + noise), each draft token drawn from q of its parent's
+    row), generated on the device for batches too large to build on the host."""
+    import torch
+
+    from long_context_speculative_gb300 import workloads as wl
+
+    g = torch.Generator(device=dev).manual_seed(w.seed * 7919 + 77)
+    z = torch.randn((B, w.n_q, w.V), generator=g, device=dev) * w.z_std
+    base = z / w.T if w.q_noise_uses_T else z
+    q = torch.softmax(base + torch.randn((B, w.n_q, w.V), generator=g, device=dev)
+                      * w.q_noise_std, dim=-1)
+    if w.tree:
+        gt = wl.gen(w.seed * 7919 + 11)
+        parents = torch.tensor([wl.random_tree(w.n_q, w.tree_nodes_max_depth, gt)
+                                for _ in range(B)], dtype=torch.int64)
+    else:
+        parents = torch.tensor([wl.chain_parents(w.n_q)] * B, dtype=torch.int64)
+    rows = parents[:, 1:].clamp(min=0).to(dev)                    # parent row of nodes 1..n_q-1
+    src = torch.gather(q, 1, rows[:, :, None].expand(B, w.n_q - 1, w.V))
+    tok = torch.zeros((B, w.n_q), dtype=torch.int32, device=dev)
+    tok[:, 1:] = torch.multinomial(src.reshape(-1, w.V), 1, generator=g).view(B, w.n_q - 1).int()
+    par = None
+    if w.tree:
+        par = parents.to(torch.int32)
+        par[:, 0] = -1
+        par = par.to(dev)
+    return z.contiguous(), q.contiguous(), tok, par
+
+
 def accept_batch_roofline(w, dev, stream, reps=20, B=None, ragged=False):
     """rapid_accept alone on a batch of at least 100 MB of z + q (larger than L2):
     the workload's own batch when that is large enough (the 4-sequence tree of
@@ -637,9 +671,12 @@ def accept_batch_roofline(w, dev, stream, reps=20, B=None, ragged=False):
         Bb = w.B
     else:
         Bb = max(16, -(-100_000_000 // (w.n_q * w.V * 8)))
-    inp = wl.accept_inputs(w, B=Bb, parents=None if not w.tree else None)
-    z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
-    par = None if inp.parent is None else inp.parent.to(dev)
+    if Bb * w.n_q * w.V * 8 > 1_000_000_000:
+        z, q, tok, par = _device_accept_inputs(w, Bb, dev)
+    else:
+        inp = wl.accept_inputs(w, B=Bb)
+        z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
+        par = None if inp.parent is None else inp.parent.to(dev)
     nbytes = z.numel() * 4 + q.numel() * 4
     nn = None
     if ragged:
