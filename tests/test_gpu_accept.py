@@ -169,6 +169,10 @@ def test_ragged_drafts_through_rapid_accept_ex(case):
     inp = wl.accept_inputs(w, T=1.0, B=len(n_nodes))
     z, q, tok = _garbage_padding(inp.z, inp.q, inp.tokens, n_nodes, seed=3)
     par = inp.parent
+    if par is not None:   # padding parents out of range too
+        par = par.clone()
+        for b, n in enumerate(n_nodes):
+            par[b, n:] = torch.tensor([-5, 1000], dtype=torch.int32).repeat(w.n_q)[:w.n_q - n]
     nn_d = torch.from_numpy(n_nodes).to(DEV)
     seen_bonus = 0
     for seed in (11, 12, 13):

@@ -346,8 +346,13 @@ def test_ragged_drafts_equal_truncated_batches(tree):
     n_nodes = np.array([4, n_q, 1, 4, 7, 2], np.int32)
     rng = np.random.default_rng(5)
     zg, qg, tg = _garbage_padding(z, q, tok, n_nodes, rng)
+    pg = None
+    if par is not None:   # padding parents out of range as well
+        pg = par.copy()
+        for b, n in enumerate(n_nodes):
+            pg[b, n:] = -5
     for seed in range(12):
-        res = oracle.accept(zg, qg, tg, par, T=1.0, eta=1.0, seed=seed, n_nodes=n_nodes)
+        res = oracle.accept(zg, qg, tg, pg, T=1.0, eta=1.0, seed=seed, n_nodes=n_nodes)
         for m in sorted(set(n_nodes.tolist())):
             ref = oracle.accept(z[:, :m], q[:, :m], tok[:, :m],
                                 None if par is None else par[:, :m], T=1.0, eta=1.0, seed=seed)
