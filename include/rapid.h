@@ -29,6 +29,9 @@
  *                      one batch and a Philox key in device memory (CUDA-graph
  *                      replays); rapid_accept_noalloc needs no workspace.
  *
+ *   rapid_attn_merge   the log-sum-exp combine of attention parts computed
+ *                      separately (shards of the key range, other devices).
+ *
  *   rapid_kv_commit    after acceptance, the accepted path's speculative K/V
  *   rapid_kv_advance   rows join the history next to the root, and the
  *                      history lengths grow by 1 + n_accepted.
@@ -126,6 +129,8 @@ size_t rapid_verify_attn_workspace_size(int B, int Hq, int Hkv, int d, int n_q,
  *             speculative row j iff spec_mask[b][i][j] != 0 (a token tree's
  *             ancestor-or-self mask).  NULL means the causal chain j <= i.
  *             Every history row is visible to every query (no mask there).
+ *             A query that sees no row at all (no history, mask row all
+ *             zero) gets O = 0 and LSE = -inf.
  *  softmax_scale  score multiplier; <= 0 selects 1/sqrt(d).
  *  O          [B, Hq, n_q, d] dtype: softmax-weighted sum of the visible V rows.
  *  LSE        float [B, Hq, n_q]: natural-log log-sum-exp of the scaled scores
@@ -144,6 +149,39 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
                                const uint8_t* spec_mask, float softmax_scale,
                                void* O, float* LSE, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/*
+ * Log-sum-exp merge of attention results computed separately over disjoint
+ * key sets: the combine step of hybrid tree attention ("LongSpec ...",
+ * section 2.3: the history part and the speculative part are combined
+ * through their log-sum-exp), for any number of parts.  With L_p the LSE and
+ * O_p the normalised output of part p:
+ *     LSE = ln sum_p exp(L_p),   O = sum_p exp(L_p - LSE) O_p.
+ * rapid_verify_attn does this for its own splits; this call merges results
+ * produced elsewhere, for example the shards of a history split by key range
+ * (each shard a rapid_verify_attn call on its rows, the speculative rows
+ * visible in exactly one of them: an all-zero spec_mask hides them from the
+ * others), possibly computed on other devices and copied here.
+ *
+ *  O_parts    device [n_parts, rows, d] of dtype: each part's O, rows
+ *             flattened (a rapid_verify_attn output is [B, Hq, n_q, d]:
+ *             rows = B * Hq * n_q).
+ *  LSE_parts  device float [n_parts, rows]: each part's natural-log LSE,
+ *             finite or -inf (-inf: the part saw no key for that row; its O
+ *             is not read).
+ *  dtype      RAPID_DTYPE_BF16 or RAPID_DTYPE_F32 (O_parts and O).
+ *  d          64 or 128.
+ *  O, LSE     device outputs [rows, d] of dtype and float [rows].  A row with
+ *             no finite part gets O = 0, LSE = -inf.
+ *
+ * Arithmetic in fp32.  Errors: RAPID_EINVAL for NULL pointers, n_parts < 1,
+ * rows < 1 or above 2^36, d not 64 or 128, a bad dtype, O_parts or O not
+ * 16-byte aligned, LSE arrays not 4-byte aligned; RAPID_ECUDA when the
+ * launch fails.
+ */
+rapid_status rapid_attn_merge(const void* O_parts, const float* LSE_parts, int dtype,
+                              int n_parts, int64_t rows, int d, void* O, float* LSE,
+                              void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Acceptance                                                                */

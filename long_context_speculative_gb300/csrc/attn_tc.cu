@@ -416,14 +416,18 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 rescale = (k_local > 0);
                 m_run = mt;
             }
+            // a row that has seen no visible key yet (a speculative tile whose
+            // mask hides every key from it, with no history before it) keeps
+            // p = 0 instead of exp(-inf + inf)
+            const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float p0 = ex2(fmaf(sv[2 * j], c, -m_run));
-                const float p1 = ex2(fmaf(sv[2 * j + 1], c, -m_run));
-                const float p2 = ex2(fmaf(sv[2 * j + 2], c, -m_run));
-                const float p3 = ex2(fmaf(sv[2 * j + 3], c, -m_run));
+                const float p0 = ex2(fmaf(sv[2 * j], c, neg_m));
+                const float p1 = ex2(fmaf(sv[2 * j + 1], c, neg_m));
+                const float p2 = ex2(fmaf(sv[2 * j + 2], c, neg_m));
+                const float p3 = ex2(fmaf(sv[2 * j + 3], c, neg_m));
                 s0 += p0; s1 += p1; s2 += p2; s3 += p3;
                 pk[j] = pack_bf16x2(p0, p1);
                 pk[j + 1] = pack_bf16x2(p2, p3);

@@ -8,6 +8,7 @@
 #include "common.cuh"
 #include "kv_commit.cuh"
 #include "lm_head.cuh"
+#include "lse_merge.cuh"
 #include "retrieval.cuh"
 #include "rapid.h"
 
@@ -202,6 +203,22 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
     if (e != cudaSuccess) return RAPID_ECUDA;
     e = launch_attn_merge(p, dtype, st);
     return e == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
+}
+
+rapid_status rapid_attn_merge(const void* O_parts, const float* LSE_parts, int dtype,
+                              int n_parts, int64_t rows, int d, void* O, float* LSE,
+                              void* stream) {
+    if (!O_parts || !LSE_parts || !O || !LSE) return RAPID_EINVAL;
+    if (dtype != RAPID_DTYPE_F32 && dtype != RAPID_DTYPE_BF16) return RAPID_EINVAL;
+    if (n_parts < 1 || rows < 1 || (d != 64 && d != 128)) return RAPID_EINVAL;
+    if (rows > (int64_t)1 << 36) return RAPID_EINVAL;
+    if (!aligned16(O_parts) || !aligned16(O) || (reinterpret_cast<uintptr_t>(LSE_parts) & 3u) ||
+        (reinterpret_cast<uintptr_t>(LSE) & 3u))
+        return RAPID_EINVAL;
+    return launch_lse_merge(O_parts, LSE_parts, dtype == RAPID_DTYPE_BF16, n_parts, rows, d, O, LSE,
+                            static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? RAPID_OK
+               : RAPID_ECUDA;
 }
 
 size_t rapid_accept_workspace_size(int B, int n_q, int V) {

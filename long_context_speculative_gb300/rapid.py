@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
     L.rapid_verify_attn.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, vp, vp, f32,
                                     vp, vp, vp, sz, vp]
     L.rapid_verify_attn.restype = i32
+    L.rapid_attn_merge.argtypes = [vp, vp, i32, i32, i64, i32, vp, vp, vp]
+    L.rapid_attn_merge.restype = i32
     L.rapid_accept_workspace_size.argtypes = [i32, i32, i32]
     L.rapid_accept_workspace_size.restype = sz
     L.rapid_accept.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp, vp, vp,
@@ -138,6 +140,21 @@ def rapid_verify_attn(Q, Kcache, Vcache, prefix_len, spec_mask, softmax_scale, O
                                  float(softmax_scale), _ptr(O), _ptr(LSE), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "rapid_verify_attn")
+
+
+def rapid_attn_merge(O_parts, LSE_parts, O, LSE, stream=None):
+    """Log-sum-exp merge of n_parts attention results: O_parts [n_parts, ..., d] (bf16 or
+    fp32), LSE_parts [n_parts, ...] float32 -> O [..., d], LSE [...]."""
+    _need_cuda(O_parts, LSE_parts, O, LSE)
+    n_parts, d = O_parts.shape[0], O_parts.shape[-1]
+    rows = LSE_parts[0].numel()
+    if (LSE_parts.dtype != torch.float32 or LSE.dtype != torch.float32 or O.dtype != O_parts.dtype
+            or O_parts.numel() != n_parts * rows * d or O.numel() != rows * d
+            or LSE.numel() != rows):
+        raise RapidError("rapid_attn_merge: mismatched shapes or dtypes")
+    st = lib().rapid_attn_merge(_ptr(O_parts), _ptr(LSE_parts), _dtype_code(O_parts), n_parts,
+                                rows, d, _ptr(O), _ptr(LSE), _stream(stream))
+    _check(st, "rapid_attn_merge")
 
 
 def rapid_accept_workspace_size(B, n_q, V) -> int:

@@ -69,6 +69,7 @@ def lib():
         L.orc_kd_grad.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_double, _dp]
         L.orc_distilled_logits.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_double,
                                            ctypes.c_double, _dp]
+        L.orc_lse_merge.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_int64, ctypes.c_int, _dp, _dp]
         L.orc_accept.argtypes = [_fp, _fp, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_int,
                                  ctypes.c_double, ctypes.c_double, ctypes.c_uint64, ctypes.c_int,
@@ -191,6 +192,20 @@ def verify_attn_split(Q, K, V, prefix_len, cuts, mask=None, scale=None, dtype=DT
 # --------------------------------------------------------------------------
 # Acceptance
 # --------------------------------------------------------------------------
+
+def lse_merge(O_parts, LSE_parts):
+    """Log-sum-exp combine of attention parts: O_parts [P, ..., d], LSE_parts [P, ...]
+    -> (O [..., d], LSE [...]) in double."""
+    Op = _c(O_parts, np.float64)
+    Lp = _c(LSE_parts, np.float64)
+    P, d = Op.shape[0], Op.shape[-1]
+    rows = Lp[0].size
+    assert Op.size == P * rows * d and Lp.size == P * rows
+    O = np.zeros(Lp.shape[1:] + (d,), np.float64)
+    L = np.zeros(Lp.shape[1:], np.float64)
+    lib().orc_lse_merge(_ptr(Op, _dp), _ptr(Lp, _dp), P, rows, d, _ptr(O, _dp), _ptr(L, _dp))
+    return O, L
+
 
 def row_dists(z, q, T, eta, clamp=True):
     """(p, p_hat unclamped, p_hat after the tail rule) of one vocabulary row."""

@@ -624,6 +624,36 @@ void orc_verify_attn_split(const void* Q, const void* K, const void* V, int dtyp
     });
 }
 
+// Log-sum-exp combine of parts computed over disjoint key sets ("LongSpec",
+// section 2.3, Hybrid Tree Attention: parts combined through their
+// log-sum-exp), written out for any number of parts: LSE = ln sum_p
+// exp(LSE_p), O = sum_p exp(LSE_p - LSE) O_p.  Parts with LSE_p = -inf saw
+// no key and add nothing; a row with no such part gets O = 0, LSE = -inf.
+void orc_lse_merge(const double* O_parts, const double* LSE_parts, int n_parts, int64_t rows,
+                   int d, double* O, double* LSE) {
+    const double ninf = -std::numeric_limits<double>::infinity();
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = ninf;
+        for (int p = 0; p < n_parts; ++p) m = std::max(m, LSE_parts[(int64_t)p * rows + r]);
+        for (int k = 0; k < d; ++k) O[r * d + k] = 0.0;
+        if (m == ninf) {
+            LSE[r] = ninf;
+            continue;
+        }
+        double s = 0.0;
+        for (int p = 0; p < n_parts; ++p) s += std::exp(LSE_parts[(int64_t)p * rows + r] - m);
+        const double L = m + std::log(s);
+        LSE[r] = L;
+        for (int p = 0; p < n_parts; ++p) {
+            const double lp = LSE_parts[(int64_t)p * rows + r];
+            if (lp == ninf) continue;
+            const double w = std::exp(lp - L);
+            const double* op = O_parts + ((int64_t)p * rows + r) * d;
+            for (int k = 0; k < d; ++k) O[r * d + k] += w * op[k];
+        }
+    }
+}
+
 // p, unclamped p_hat and (optionally clamped) p_hat of one row.
 void orc_row_dists(const float* z, const float* q, int V, double T, double eta, int clamp,
                    double* p, double* phat_raw, double* phat) {

@@ -177,3 +177,80 @@ def test_rows_entry_matches_full():
     for n, (b, h, i) in enumerate(rows):
         np.testing.assert_array_equal(Or[n], O[b, h, i])
         assert Lr[n] == L[b, h, i]
+
+
+def _shards(K, V, pl, n_q, cuts):
+    """Caches of the history pieces [cuts[k], cuts[k+1]) of every sequence,
+    each followed by the sequence's n_q speculative rows (moved up after the
+    piece); returns [(K_k, V_k, prefix_k)]."""
+    B, Hkv, cap, d = K.shape
+    out = []
+    for k in range(len(cuts) - 1):
+        Kk = np.zeros_like(K)
+        Vk = np.zeros_like(V)
+        pk = np.zeros(B, np.int32)
+        for b in range(B):
+            lo, hi = min(cuts[k], pl[b]), min(cuts[k + 1], pl[b])
+            n = hi - lo
+            Kk[b, :, :n] = K[b, :, lo:hi]
+            Vk[b, :, :n] = V[b, :, lo:hi]
+            Kk[b, :, n:n + n_q] = K[b, :, pl[b]:pl[b] + n_q]
+            Vk[b, :, n:n + n_q] = V[b, :, pl[b]:pl[b] + n_q]
+            pk[b] = n
+        out.append((Kk, Vk, pk))
+    return out
+
+
+@pytest.mark.parametrize("tree", [False, True])
+def test_lse_merge_of_key_shards_equals_unsplit(tree):
+    # Shards of the history by key range (one of them empty), the speculative
+    # rows visible only in the last shard (an all-zero mask hides them from
+    # the others): merging the shards' (O, LSE) gives the unsplit attention.
+    B, Hq, Hkv, d, n_q, cap = 2, 4, 2, 64, 6, 400
+    Q, K, V = _rand(B, Hq, Hkv, d, n_q, cap, 31)
+    pl = np.array([300, 170], np.int32)
+    if tree:
+        parents = [wl.random_tree(n_q, 3, wl.gen(40 + b)) for b in range(B)]
+        mask = np.stack([wl.ancestor_mask(p).numpy() for p in parents])
+    else:
+        mask = np.stack([np.tril(np.ones((n_q, n_q), np.uint8))] * B)
+    O_ref, L_ref = oracle.verify_attn(Q, K, V, pl, mask)
+    cuts = [0, 100, 100, 230, 400]
+    shards = _shards(K, V, pl, n_q, cuts)
+    none = np.zeros_like(mask)
+    parts = [oracle.verify_attn(Q, Kk, Vk, pk, mask if k == len(shards) - 1 else none)
+             for k, (Kk, Vk, pk) in enumerate(shards)]
+    # the empty piece of sequence 1 (rows 230..) and the repeated cut give
+    # parts that saw no key: LSE -inf, O 0
+    assert np.isneginf(parts[1][1]).all() and (parts[1][0] == 0).all()
+    O, L = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(O, O_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L, L_ref, rtol=0, atol=1e-12)
+
+
+def test_lse_merge_closed_forms():
+    rng = np.random.default_rng(4)
+    O1 = rng.standard_normal((3, 5, 8))
+    L1 = rng.standard_normal((3, 5))
+    # one part: itself
+    O, L = oracle.lse_merge(O1[None], L1[None])
+    np.testing.assert_array_equal(O, O1)
+    np.testing.assert_array_equal(L, L1)
+    # the same part twice: the same O, LSE + ln 2
+    O, L = oracle.lse_merge(np.stack([O1, O1]), np.stack([L1, L1]))
+    np.testing.assert_allclose(O, O1, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(L, L1 + math.log(2.0), rtol=1e-14)
+    # a part that saw no key adds nothing, whatever its O holds
+    O, L = oracle.lse_merge(np.stack([O1, np.full_like(O1, 1e30)]),
+                            np.stack([L1, np.full_like(L1, -np.inf)]))
+    np.testing.assert_array_equal(O, O1)
+    np.testing.assert_array_equal(L, L1)
+    # no part at all: O = 0, LSE = -inf
+    O, L = oracle.lse_merge(np.stack([O1, O1]), np.full((2, 3, 5), -np.inf))
+    assert (O == 0).all() and np.isneginf(L).all()
+    # two parts with LSE a and b: weights e^a / (e^a + e^b) and e^b / (e^a + e^b)
+    a, b = 0.3, -1.2
+    O, L = oracle.lse_merge(np.array([[[1.0, 0.0]], [[0.0, 1.0]]]), np.array([[a], [b]]))
+    wa = 1.0 / (1.0 + math.exp(b - a))
+    np.testing.assert_allclose(O[0], [wa, 1.0 - wa], rtol=1e-14)
+    np.testing.assert_allclose(L[0], a + math.log1p(math.exp(b - a)), rtol=1e-14)
