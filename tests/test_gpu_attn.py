@@ -125,6 +125,26 @@ def test_llama8b_120k_layer_sampled_rows():
     check_attn(Og, Lg, Oo, Lo)
 
 
+@pytest.mark.parametrize("name", ["llama70b_128k", "llama8b_decode_120k"])
+def test_other_full_size_shapes_sampled_rows(name):
+    # one layer of the 64/8-head 128K shape (88 group rows: the 128-row
+    # configuration) and of the single-query decode shape (4 group rows)
+    w = {"llama70b_128k": wl.LLAMA70B_128K, "llama8b_decode_120k": wl.LLAMA8B_DECODE_120K}[name]
+    a = wl.attn_inputs(w, device=DEV, layer=1)
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    n = 24
+    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n), rng.integers(0, w.n_q, n)], 1)
+    Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
+                                     a.prefix_len.cpu().numpy(), rows, dtype=oracle.DTYPE_BF16)
+    Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    check_attn(Og, Lg, Oo, Lo)
+    del a
+    torch.cuda.empty_cache()
+
+
 def test_qwen_tree_shape_sampled_rows():
     w = wl.QWEN7B_TREE
     a = wl.attn_inputs(w, device=DEV, layer=0)
