@@ -37,7 +37,8 @@
  *                      history lengths grow by 1 + n_accepted.
  *
  *   rapid_lm_head      the target's logits of the verify rows from the shared
- *   rapid_lm_head_accept  LM head, alone or followed by rapid_accept.
+ *   rapid_lm_head_accept  LM head, alone or followed by rapid_accept (or, with
+ *                      rapid_lm_head_accept_ex, by rapid_accept_ex).
  *
  *   rapid_retrieval_scores  cosine scores of chunk embeddings against the
  *   rapid_retrieval_select  query, and the budgeted, thresholded choice of
@@ -506,6 +507,21 @@ rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidd
                                   uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
                                   int32_t* next_token, int32_t* path, float* diag,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * rapid_lm_head_accept with rapid_accept_ex's two optional device inputs:
+ * per-sequence node counts n_nodes (the logits of every row are still
+ * computed) and the Philox key at philox_seed_dev.  Same workspace size as
+ * rapid_lm_head_accept; the errors of both calls.
+ */
+rapid_status rapid_lm_head_accept_ex(const void* hidden, const void* W_lm, int hidden_dim,
+                                     const float* q_draft, const int32_t* draft_tokens,
+                                     const int32_t* parent, const int32_t* n_nodes, int B,
+                                     int n_q, int V, float T, float eta, uint64_t philox_seed,
+                                     const uint64_t* philox_seed_dev, uint32_t flags,
+                                     int32_t* n_accepted, int32_t* next_token, int32_t* path,
+                                     float* diag, void* workspace, size_t workspace_bytes,
+                                     void* stream);
 
 
 #ifdef __cplusplus

@@ -296,12 +296,14 @@ size_t rapid_lm_head_accept_workspace_size(int B, int n_q, int V) {
     return align_up((size_t)B * n_q * V * sizeof(float)) + acc;
 }
 
-rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidden_dim,
-                                  const float* q_draft, const int32_t* draft_tokens,
-                                  const int32_t* parent, int B, int n_q, int V, float T, float eta,
-                                  uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
-                                  int32_t* next_token, int32_t* path, float* diag,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+static rapid_status lm_head_accept_impl(const void* hidden, const void* W_lm, int hidden_dim,
+                                        const float* q_draft, const int32_t* draft_tokens,
+                                        const int32_t* parent, const int32_t* n_nodes, int B,
+                                        int n_q, int V, float T, float eta, uint64_t philox_seed,
+                                        const uint64_t* philox_seed_dev, uint32_t flags,
+                                        int32_t* n_accepted, int32_t* next_token, int32_t* path,
+                                        float* diag, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
     if (!hidden || !W_lm || !q_draft || !draft_tokens || !n_accepted || !next_token || !workspace)
         return RAPID_EINVAL;
     if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return RAPID_EINVAL;
@@ -312,6 +314,8 @@ rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidd
     if (!aligned16(hidden) || !aligned16(W_lm) || (reinterpret_cast<uintptr_t>(q_draft) & 3u) ||
         !aligned16(workspace))
         return RAPID_EINVAL;
+    if (philox_seed_dev && (reinterpret_cast<uintptr_t>(philox_seed_dev) & 7u)) return RAPID_EINVAL;
+    if (n_nodes && (reinterpret_cast<uintptr_t>(n_nodes) & 3u)) return RAPID_EINVAL;
     if (workspace_bytes < rapid_lm_head_accept_workspace_size(B, n_q, V)) return RAPID_ENOMEM;
     if (!lm_head_supported()) return RAPID_EUNSUPPORTED;
     // z lives at the front of the workspace (B n_q V floats, L2-resident at
@@ -322,8 +326,34 @@ rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidd
     if (launch_lm_head(hidden, W_lm, B * n_q, hidden_dim, V, z, device_error_word(), st) !=
         cudaSuccess)
         return RAPID_ECUDA;
-    return accept_launch(z, q_draft, draft_tokens, parent, B, n_q, nullptr, V, T, eta, philox_seed,
-                         nullptr, flags, n_accepted, next_token, path, diag, acc_ws, st);
+    return accept_launch(z, q_draft, draft_tokens, parent, B, n_q, n_nodes, V, T, eta,
+                         philox_seed, philox_seed_dev, flags, n_accepted, next_token, path, diag,
+                         acc_ws, st);
+}
+
+rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidden_dim,
+                                  const float* q_draft, const int32_t* draft_tokens,
+                                  const int32_t* parent, int B, int n_q, int V, float T, float eta,
+                                  uint64_t philox_seed, uint32_t flags, int32_t* n_accepted,
+                                  int32_t* next_token, int32_t* path, float* diag,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    return lm_head_accept_impl(hidden, W_lm, hidden_dim, q_draft, draft_tokens, parent, nullptr,
+                               B, n_q, V, T, eta, philox_seed, nullptr, flags, n_accepted,
+                               next_token, path, diag, workspace, workspace_bytes, stream);
+}
+
+rapid_status rapid_lm_head_accept_ex(const void* hidden, const void* W_lm, int hidden_dim,
+                                     const float* q_draft, const int32_t* draft_tokens,
+                                     const int32_t* parent, const int32_t* n_nodes, int B,
+                                     int n_q, int V, float T, float eta, uint64_t philox_seed,
+                                     const uint64_t* philox_seed_dev, uint32_t flags,
+                                     int32_t* n_accepted, int32_t* next_token, int32_t* path,
+                                     float* diag, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+    return lm_head_accept_impl(hidden, W_lm, hidden_dim, q_draft, draft_tokens, parent, n_nodes,
+                               B, n_q, V, T, eta, philox_seed, philox_seed_dev, flags,
+                               n_accepted, next_token, path, diag, workspace, workspace_bytes,
+                               stream);
 }
 
 const char* rapid_status_string(int status) {

@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
     L.rapid_lm_head_accept.argtypes = [vp, vp, i32, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32,
                                        vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.rapid_lm_head_accept.restype = i32
+    L.rapid_lm_head_accept_ex.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, f32, f32,
+                                          u64, vp, u32, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.rapid_lm_head_accept_ex.restype = i32
     _lib = L
     return L
 
@@ -238,6 +241,33 @@ def rapid_lm_head_accept(hidden, W_lm, q_draft, draft_tokens, parent, T, eta, ph
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream))
     _check(st, "rapid_lm_head_accept")
+
+
+def rapid_lm_head_accept_ex(hidden, W_lm, q_draft, draft_tokens, parent, n_nodes, T, eta,
+                            philox_seed, flags, n_accepted, next_token, path, diag, workspace,
+                            stream=None):
+    """rapid_lm_head_accept with rapid_accept_ex's node counts and device Philox key
+    (philox_seed: an int, or a one-element 64-bit integer CUDA tensor)."""
+    _need_cuda(hidden, W_lm, q_draft, draft_tokens, parent, n_nodes, n_accepted, next_token,
+               path, diag, workspace)
+    B, n_q, V = q_draft.shape
+    if n_nodes is not None and (n_nodes.dtype != torch.int32 or n_nodes.numel() != B):
+        raise RapidError("n_nodes must be an int32 tensor of B entries")
+    if isinstance(philox_seed, torch.Tensor):
+        _need_cuda(philox_seed)
+        if philox_seed.dtype not in (torch.int64, torch.uint64) or philox_seed.numel() != 1:
+            raise RapidError("a device philox_seed must be a one-element 64-bit integer tensor")
+        key, key_dev = 0, _ptr(philox_seed)
+    else:
+        key, key_dev = int(philox_seed) & ((1 << 64) - 1), None
+    st = lib().rapid_lm_head_accept_ex(_ptr(hidden), _ptr(W_lm), hidden.shape[1], _ptr(q_draft),
+                                       _ptr(draft_tokens), _ptr(parent), _ptr(n_nodes), B, n_q,
+                                       V, float(T), float(eta), key, key_dev, int(flags),
+                                       _ptr(n_accepted), _ptr(next_token), _ptr(path),
+                                       _ptr(diag), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _check(st, "rapid_lm_head_accept_ex")
 
 
 class KVLayerTable:

@@ -163,3 +163,34 @@ def test_fused_equals_logits_then_accept():
     torch.cuda.synchronize()
     for k in ("n_accepted", "next_token", "path", "diag"):
         assert torch.equal(a[k], b[k]), k
+
+
+def test_fused_ex_equals_logits_then_accept_ex():
+    # node counts and a device key through the fused call give what rapid_lm_head
+    # followed by rapid_accept_ex gives, bit for bit
+    B, n_q, hidden, V = 3, 11, 512, 20000
+    H, W = _weights(B * n_q, hidden, V, seed=19)
+    Hd, Wd = H.to(DEV), W.to(DEV)
+    z_ref = oracle.lm_head_logits(H.float().numpy(), W.float().numpy()).reshape(B, n_q, V)
+    q, tokens = _draft_from_logits(z_ref, None, 1.0, 20)
+    qd, td = torch.from_numpy(q).to(DEV), torch.from_numpy(tokens).to(DEV)
+    nn = torch.tensor([11, 4, 1], dtype=torch.int32, device=DEV)
+    key = torch.tensor([0x0123_4567_89AB], dtype=torch.int64, device=DEV)
+    z = torch.empty((B * n_q, V), dtype=torch.float32, device=DEV)
+    rapid.rapid_lm_head(Hd, Wd, z)
+    a = rapid.accept(z.view(B, n_q, V), qd, td, None, T=1.0, eta=1.0, seed=key, n_nodes=nn)
+    outs = dict(n_accepted=torch.empty(B, dtype=torch.int32, device=DEV),
+                next_token=torch.empty(B, dtype=torch.int32, device=DEV),
+                path=torch.empty((B, n_q), dtype=torch.int32, device=DEV),
+                diag=torch.empty((B, n_q, 5), dtype=torch.float32, device=DEV))
+    ws = torch.empty(rapid.rapid_lm_head_accept_workspace_size(B, n_q, V), dtype=torch.uint8,
+                     device=DEV)
+    rapid.rapid_lm_head_accept_ex(Hd, Wd, qd, td, None, nn, 1.0, 1.0, key,
+                                  rapid.RAPID_ACCEPT_TAIL_CLAMP, outs["n_accepted"],
+                                  outs["next_token"], outs["path"], outs["diag"], ws)
+    torch.cuda.synchronize()
+    for k in ("n_accepted", "next_token", "path"):
+        assert torch.equal(a[k], outs[k]), k
+    real = torch.arange(n_q, device=DEV)[None, :] < nn[:, None]
+    assert torch.equal(a["diag"][real], outs["diag"][real])
+    assert rapid.rapid_device_error(True) == 0
