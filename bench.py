@@ -708,6 +708,18 @@ def accept_batch_roofline(w, dev, stream, reps=20, B=None, ragged=False):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
+    # the same calls replayed from a CUDA graph (no host launch cost between them)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(reps):
+            call(200 + i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph = e0.elapsed_time(e1) / reps
     achieved = nbytes / (ms * 1e-3) / 1e9
     peak, src = _peaks()
     if nn is None:
@@ -718,7 +730,8 @@ def accept_batch_roofline(w, dev, stream, reps=20, B=None, ragged=False):
     return {"bound": "hbm", "kernel": "rapid_accept (row + select kernels)",
             "batch": batch,
             "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "avg_launch_ms": ms, "peak_source": src + " (hbm_gbs, copy)"}
+            "avg_launch_ms": ms, "avg_launch_ms_graph": ms_graph,
+            "peak_source": src + " (hbm_gbs, copy)"}
 
 
 def profile_accept(w, B):
