@@ -21,9 +21,16 @@ struct AttnParams {
     const uint8_t* mask;  // [B, n_q, n_q] or nullptr (chain)
     void* O;              // [B, Hq, n_q, d]
     float* LSE;           // [B, Hq, n_q]
-    float* part_acc;      // [B*Hkv, nparts, R, d]   un-normalised partial outputs
-    float* part_ml;       // [B*Hkv, nparts, R, 2]   (running max m, sum l), log2 domain
+    // Partials: un-normalised outputs (part_acc, d floats per row) and their
+    // (running max m, sum l) in the log2 domain (part_ml, 2 floats per row).
+    // CUDA-core kernel: [B*Hkv, nparts, R, .] (every sequence has nparts
+    // splits).  Tensor-core kernel: [Hkv, nparts, R, .] by the launch's
+    // (sequence, split) slot, nparts = the slots per KV head; sequence b's
+    // S_b splits sit at slots part_first[b*Hkv+g] .. + part_nsplit[b*Hkv+g] - 1.
+    float* part_acc;
+    float* part_ml;
     int* part_nsplit;     // [B*Hkv] splits written per (b, KV head) by the tensor-core kernel
+    int* part_first;      // [B*Hkv] first slot of those splits
     unsigned int* err;    // sticky device error word
     int64_t cap;          // KV rows per head
     int64_t chunk;        // history rows per split (multiple of 128)

@@ -203,11 +203,14 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     const int g = bg % p.Hkv;
     const int h = g * p.G + r / p.n_q;
     const int i = r % p.n_q;
-    // partial slots written for this sequence: all S for the CUDA-core
-    // history kernel; S_b of the balanced plan for the tensor-core kernel
+    // partial slots written for this sequence: all S of (b, g) for the
+    // CUDA-core history kernel; the S_b slots from part_first for the
+    // tensor-core kernel
     const int nparts = p.balanced ? p.part_nsplit[bg] : p.nparts;
-    const float* ml = p.part_ml + ((int64_t)bg * p.nparts * p.R + r) * 2;     // + s * R * 2
-    const float* pa = p.part_acc + ((int64_t)bg * p.nparts * p.R + r) * D;    // + s * R * D
+    const int64_t first = p.balanced ? (int64_t)g * p.nparts + p.part_first[bg]
+                                     : (int64_t)bg * p.nparts;
+    const float* ml = p.part_ml + (first * p.R + r) * 2;     // + s * R * 2
+    const float* pa = p.part_acc + (first * p.R + r) * D;    // + s * R * D
     const int64_t mls = (int64_t)p.R * 2, pas = (int64_t)p.R * D;
 
     // ---- speculative rows (warp 0), only when the history kernel skipped them
@@ -330,7 +333,9 @@ cudaError_t launch_simt_typed(const AttnParams& p, cudaStream_t st) {
 
 template <typename T, int D>
 cudaError_t launch_merge_typed(const AttnParams& p, cudaStream_t st) {
-    if (p.nparts > kMergeMaxS) return cudaErrorNotSupported;
+    // partials per row: at most nparts for the CUDA-core kernel; S_b <=
+    // nparts - B + 1 for the tensor-core kernel (every sequence has a split)
+    if ((p.balanced ? p.nparts - p.B + 1 : p.nparts) > kMergeMaxS) return cudaErrorNotSupported;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.R, p.B * p.Hkv, 1);
     cfg.blockDim = dim3(kMergeThreads, 1, 1);

@@ -179,9 +179,11 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     if (tid == 0) {
         const SplitOf sp0 = split_of(p, p.S, slot_idx);
         bars->split = sp0;
-        // the merge kernel reads the number of partials of this (b, g) here
-        if (sp0.b >= 0 && sp0.s == 0 && rb == 0)
+        // the merge kernel reads where the partials of this (b, g) are here
+        if (sp0.b >= 0 && sp0.s == 0 && rb == 0) {
             p.part_nsplit[sp0.b * p.Hkv + g] = sp0.S_b;
+            p.part_first[sp0.b * p.Hkv + g] = slot_idx;
+        }
     }
     __syncthreads();
 
@@ -200,7 +202,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int n_hist = t_end - t_begin;
     const bool spec_here = has_work && (s == sp.S_b - 1);
     const int n = has_work ? n_hist + (spec_here ? 1 : 0) : 0;
-    const int64_t slot = ((int64_t)bg * p.nparts + s) * p.R;
+    const int64_t slot = ((int64_t)g * p.nparts + slot_idx) * p.R;   // this CTA's partial rows
 
     // Q rows of the group into shared memory (K-major, 128-byte swizzle);
     // rows >= R are zero.

@@ -45,8 +45,9 @@ int sm_count() {
 struct AttnPlan {
     bool tc;        // tensor-core history kernel
     int S;          // splits of the history per (b, kv head)
-    int nparts;     // partial slots per (b, kv head)
+    int nparts;     // partial slots per (b, kv head); per kv head for the tensor-core kernel
     int64_t chunk;  // history rows per split
+    size_t part_rows;   // partial rows in the workspace
     size_t ws_bytes;
 };
 
@@ -82,9 +83,11 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
         pl.S = (int)S;
         pl.nparts = (int)S;
         pl.chunk = 0;
-        const size_t part = (size_t)B * Hkv * pl.nparts * R;
+        // partials by launch slot: [Hkv, S, R] rows, whatever B is
+        const size_t part = (size_t)Hkv * pl.nparts * R;
+        pl.part_rows = part;
         pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float)) +
-                      align_up((size_t)B * Hkv * sizeof(int));
+                      2 * align_up((size_t)B * Hkv * sizeof(int));
         return pl;
     } else {
         const int64_t rbs = (R + 63) / 64;
@@ -106,8 +109,9 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     pl.chunk = chunk;
     pl.nparts = (int)S;
     const size_t part = (size_t)B * Hkv * pl.nparts * R;
+    pl.part_rows = part;
     pl.ws_bytes = align_up(part * d * sizeof(float)) + align_up(part * 2 * sizeof(float)) +
-                  align_up((size_t)B * Hkv * sizeof(int));
+                  2 * align_up((size_t)B * Hkv * sizeof(int));
     return pl;
 }
 
@@ -191,13 +195,15 @@ rapid_status rapid_verify_attn(const void* Q, const void* Kcache, const void* Vc
     p.err = device_error_word();
     p.scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)d);
     p.scale_log2 = p.scale * kLog2e;
-    const size_t part = (size_t)B * Hkv * pl.nparts * p.R;
-    p.part_acc = static_cast<float*>(workspace);
-    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                         align_up(part * d * sizeof(float)));
-    p.part_nsplit = reinterpret_cast<int*>(static_cast<char*>(workspace) +
-                                           align_up(part * d * sizeof(float)) +
-                                           align_up(part * 2 * sizeof(float)));
+    const size_t part = pl.part_rows;
+    char* ws = static_cast<char*>(workspace);
+    p.part_acc = reinterpret_cast<float*>(ws);
+    ws += align_up(part * d * sizeof(float));
+    p.part_ml = reinterpret_cast<float*>(ws);
+    ws += align_up(part * 2 * sizeof(float));
+    p.part_nsplit = reinterpret_cast<int*>(ws);
+    ws += align_up((size_t)B * Hkv * sizeof(int));
+    p.part_first = reinterpret_cast<int*>(ws);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = pl.tc ? launch_attn_prefix_tc(p, st) : launch_attn_prefix_simt(p, dtype, st);
     if (e != cudaSuccess) return RAPID_ECUDA;

@@ -100,6 +100,20 @@ def test_decode_single_query_ragged():
     _run_and_check(w, prefix_override=[9000, 17, 0])
 
 
+@pytest.mark.parametrize("B,Hkv,prefix,tree", [(40, 8, 900, False), (200, 2, 300, True)])
+def test_more_sequences_than_slots(B, Hkv, prefix, tree):
+    # more sequences than (sequence, split) slots per KV head (152 SMs / Hkv):
+    # every sequence gets one split, the launch runs in several waves, and the
+    # partials sit in the launch's slots
+    w = wl.Workload("t", B=B, Hq=4 * Hkv, Hkv=Hkv, d=128, n_q=8 if tree else 11, prefix=prefix,
+                    prefix_lo=0, layers=1, V=10, dtype="bf16", z_std=1, q_noise_std=1,
+                    q_noise_uses_T=True, tree=tree, tree_nodes_max_depth=4, seed=B)
+    _run_and_check(w)
+    ws = rapid.rapid_verify_attn_workspace_size(B, w.Hq, Hkv, 128, w.n_q, w.capacity,
+                                                rapid.RAPID_DTYPE_BF16)
+    assert 0 < ws < 64 << 20   # linear in B, not quadratic
+
+
 def test_custom_scale_and_fp32_d128():
     w = wl.Workload("t", B=2, Hq=6, Hkv=3, d=128, n_q=4, prefix=700, prefix_lo=650, layers=1,
                     V=10, dtype="f32", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=51)
