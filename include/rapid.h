@@ -140,7 +140,7 @@ size_t rapid_verify_attn_workspace_size(int B, int Hq, int Hkv, int d, int n_q,
  *             bytes, 256-byte aligned; contents need no initialisation.
  *
  * Errors: RAPID_EINVAL for NULL tensors, d not in {64,128}, Hq % Hkv != 0,
- * n_q outside [1, RAPID_MAX_NQ], B < 1, kv_capacity < n_q, misaligned
+ * n_q outside [1, RAPID_MAX_NQ], B < 1, B * Hkv > 65535, kv_capacity < n_q, misaligned
  * pointers (16 bytes); RAPID_ENOMEM for a short workspace; RAPID_ECUDA when a
  * launch fails.
  */

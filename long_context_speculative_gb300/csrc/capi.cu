@@ -53,6 +53,7 @@ struct AttnPlan {
 
 bool attn_args_ok(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtype) {
     if (B < 1 || Hq < 1 || Hkv < 1 || (Hq % Hkv) != 0) return false;
+    if ((int64_t)B * Hkv > 65535) return false;   // one grid dimension of the merge launch
     if (d != 64 && d != 128) return false;
     if (n_q < 1 || n_q > RAPID_MAX_NQ) return false;
     if (cap < n_q || cap > ((int64_t)1 << 31)) return false;

@@ -61,6 +61,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.rapid_verify_attn_workspace_size(1, 4, 1, 96, 5, 64, 1) == 0
     assert lib.rapid_verify_attn_workspace_size(1, 4, 1, 128, 65, 640, 1) == 0
     assert lib.rapid_verify_attn_workspace_size(1, 3, 2, 128, 5, 64, 1) == 0
+    assert lib.rapid_verify_attn_workspace_size(8192, 8, 8, 128, 5, 64, 1) == 0   # B * Hkv
     assert lib.rapid_accept_workspace_size(1, 65, 100) == 0
     assert lib.rapid_accept_workspace_size(1, 5, 229377) == 0
     assert lib.rapid_accept_workspace_size(2, 11, 128256) > 0
