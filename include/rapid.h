@@ -230,7 +230,7 @@ size_t rapid_accept_workspace_size(int B, int n_q, int V);
  * NULL (for node i >= 1: p_j(t_i), clamped p_hat_j(t_i), q_j(t_i), ratio, r_i;
  * node 0 gets zeros).
  *
- * Errors: RAPID_EINVAL for NULL required tensors, B < 1, n_q outside
+ * Errors: RAPID_EINVAL for NULL required tensors, B outside [1, 65535], n_q outside
  * [1, RAPID_MAX_NQ], V outside [1, RAPID_MAX_VOCAB], T <= 0 or not finite,
  * eta < 0 or not finite; RAPID_ENOMEM for a short workspace; RAPID_ECUDA when
  * a launch fails.

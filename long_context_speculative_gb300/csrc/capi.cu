@@ -243,6 +243,7 @@ static rapid_status accept_args(const float* z_target, const float* q_draft,
     if (!z_target || !q_draft || !draft_tokens || !n_accepted || !next_token || !workspace)
         return RAPID_EINVAL;
     if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ || V < 1 || V > RAPID_MAX_VOCAB) return RAPID_EINVAL;
+    if (B > 65535) return RAPID_EINVAL;   // one grid dimension of the selection launch
     if (!(T > 0.f) || !std::isfinite(T) || !(eta >= 0.f) || !std::isfinite(eta)) return RAPID_EINVAL;
     if ((flags & ~(uint32_t)RAPID_ACCEPT_TAIL_CLAMP) != 0) return RAPID_EINVAL;
     if ((reinterpret_cast<uintptr_t>(z_target) & 3u) || (reinterpret_cast<uintptr_t>(q_draft) & 3u))
