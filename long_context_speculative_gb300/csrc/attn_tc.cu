@@ -46,35 +46,44 @@ constexpr int kSoftmaxWarps = 8;                // two groups x four TMEM lane q
 constexpr int kProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 2;
 constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
-constexpr int kD = 128;
 constexpr int kKeys = 64;                       // keys per K/V tile
-constexpr int kMaxStages = 6;
-// TMEM columns: S of group g, buffer u at 64 (2 g + u); O of group g at 256 + 128 g.
+constexpr int kBlockBytes = kKeys * 128;        // one 64-column block of a K or V tile (8 KB)
+constexpr int kMaxStages = 12;
+// TMEM columns: S of group g, buffer u at 64 (2 g + u); O of group g at 256 + D g.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = 256;
-constexpr int kTileBytes = kKeys * kD * 2;      // 16 KB: 2 column blocks x 8 KB
-constexpr int kStageBytes = 2 * kTileBytes;     // K + V
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 
 // Shared-memory plan for ROWS query rows kept on chip (64 when the group has
-// at most 64 rows, else 128).  The MMAs always run with M = 128: with ROWS =
-// 64 the operand rows 64..127 of Q and P read the neighbouring (finite)
-// shared data and only produce output rows that are never used, which frees
-// 32 KB for a sixth K/V stage.
-template <int ROWS>
+// at most 64 rows, else 128) and head dimension D (64 or 128).  The MMAs
+// always run with M = 128: with ROWS = 64 the operand rows 64..127 of Q and P
+// read the neighbouring shared data and only produce output rows that are
+// never used, which frees room for more K/V stages.  The ring takes what
+// shared memory is left: 6 / 5 stages of 32 KB at D = 128, 12 / 11 stages of
+// 16 KB at D = 64 (the same bytes in flight).
+template <int ROWS, int D>
 struct Plan {
+    static constexpr int kD = D;
+    static constexpr int kDBlocks = D / 64;              // 64-column blocks of Q, K and V
+    static constexpr int kTileBytes = kKeys * D * 2;     // one K or V tile
+    static constexpr int kStageBytes = 2 * kTileBytes;   // K + V
     static constexpr int kActiveQuadrants = ROWS / 32;   // softmax warps per group
     static constexpr int kGroupThreads = 32 * kActiveQuadrants;
-    static constexpr int kStages = ROWS == 64 ? 6 : 5;
     static constexpr int kQBlock = ROWS * 128;           // one 64-column block of Q
     static constexpr int kPBytes = ROWS * 128;           // one P buffer (64 keys)
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + 2 * kQBlock;
+    static constexpr int kOffP = kOffQ + kDBlocks * kQBlock;
     static constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
+    static constexpr int kFit = (232448 - 1024 - kBarBytes - kOffKV) / kStageBytes;
+    static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
     static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + 1 KB alignment slack
-    static_assert(kStages <= kMaxStages, "too many stages");
+    // instruction descriptor of O += P V (V MN-major, N = D)
+    static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                         ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static_assert(kStages >= 4, "too few stages");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -83,8 +92,6 @@ struct Plan {
 // bits 24-28 = M/16.
 constexpr uint32_t kIdescS = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kKeys >> 3) << 17) |
                              ((uint32_t)(128 >> 4) << 24);
-constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                              ((uint32_t)(kD >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
 // 2^x with the SFU instruction (flushes denormal results to zero; P is
 // rounded to bf16 afterwards and the running sums tolerate the 2-ulp error).
@@ -121,11 +128,14 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= kBarBytes, "barrier block too small");
 
-template <int ROWS>
+template <int ROWS, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
-    using L = Plan<ROWS>;
+    using L = Plan<ROWS, D>;
+    constexpr int kD = L::kD;
+    constexpr int kTileBytes = L::kTileBytes;
+    constexpr int kStageBytes = L::kStageBytes;
     constexpr int kStages = L::kStages;
     constexpr int kOffQ = L::kOffQ;
     constexpr int kOffP = L::kOffP;
@@ -208,19 +218,20 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     // rows >= R are zero.
     if (tid < ROWS && n > 0) {
         const int r = tid;
-        uint4 chunk[16];
+        constexpr int kQChunks = kD / 8;   // 16-byte pieces of a Q row
+        uint4 chunk[kQChunks];
         if (r < Rb) {
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const __nv_bfloat16*>(p.Q) +
                 (((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q + r0 + r) * kD);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) chunk[j] = src[j];
+            for (int j = 0; j < kQChunks; ++j) chunk[j] = src[j];
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) chunk[j] = make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < kQChunks; ++j) chunk[j] = make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < kQChunks; ++j) {
             const int blk = j >> 3, jj = j & 7;
             *reinterpret_cast<uint4*>(smem + kOffQ + blk * L::kQBlock + r * 128 +
                                       ((jj ^ (r & 7)) << 4)) = chunk[j];
@@ -263,10 +274,11 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 uint8_t* vt = kt + kTileBytes;
                 const int y = tile_y(i);
                 mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
-                tma_load_2d(kt, &tmK, 0, y, &bars->kv_full[st]);
-                tma_load_2d(kt + kTileBytes / 2, &tmK, 64, y, &bars->kv_full[st]);
-                tma_load_2d(vt, &tmV, 0, y, &bars->kv_full[st]);
-                tma_load_2d(vt + kTileBytes / 2, &tmV, 64, y, &bars->kv_full[st]);
+#pragma unroll
+                for (int c = 0; c < L::kDBlocks; ++c) {   // 64-column blocks of K, then V
+                    tma_load_2d(kt + c * kBlockBytes, &tmK, 64 * c, y, &bars->kv_full[st]);
+                    tma_load_2d(vt + c * kBlockBytes, &tmV, 64 * c, y, &bars->kv_full[st]);
+                }
             }
             if (*((volatile int*)&bars->abort)) {
                 // let the copies still in flight land before the CTA exits
@@ -288,7 +300,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             const uint64_t qd0 = sdesc(smem_base + kOffQ, 16, 1024);
             const uint64_t kd0 = sdesc(smem_base + kOffKV, 16, 1024);
             const uint64_t pd0 = sdesc(smem_base + kOffP, 16, 1024);
-            const uint64_t vd0 = sdesc(smem_base + kOffKV + kTileBytes, kTileBytes / 2, 1024);
+            const uint64_t vd0 = sdesc(smem_base + kOffKV + kTileBytes, kBlockBytes, 1024);
             int next_s = 0, next_pv = 0;
             bool ok = true;
             uint64_t t_last = global_timer_ns();
@@ -323,7 +335,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
                     for (int k = 0; k < kKeys / 16; ++k) {
                         mma_bf16(dO, pd + (uint64_t)(k * 2), vd + (uint64_t)(k * (2048 >> 4)),
-                                 kIdescPV, (i > 1 || k > 0) ? 1u : 0u);
+                                 L::kIdescPV, (i > 1 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(&bars->p_free[gr]);
                     mma_commit(&bars->kv_empty[st]);
@@ -495,13 +507,14 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             // tcgen05.ld is warp-collective (.sync.aligned): every lane
             // executes the same loads; only the stores are per-row.
             const bool real_row = r < Rb;
-            const int half = gr;                      // this warp's 64 output columns
-            float* dst = p.part_acc + (slot + r0 + r) * kD + half * 64;
+            const int half = gr;                      // this warp's D / 2 output columns
+            const int c0 = half * (kD / 2);
+            float* dst = p.part_acc + (slot + r0 + r) * kD + c0;
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
+            for (int qq = 0; qq < kD / 64; ++qq) {
                 uint32_t o0[32], o1[32];
-                tmem_ld32(lane_addr + kTmemO + half * 64 + qq * 32, o0);
-                tmem_ld32(lane_addr + kTmemO + kD + half * 64 + qq * 32, o1);
+                tmem_ld32(lane_addr + kTmemO + c0 + qq * 32, o0);
+                tmem_ld32(lane_addr + kTmemO + kD + c0 + qq * 32, o1);
                 tmem_wait_ld();
                 if (real_row) {
 #pragma unroll
@@ -532,12 +545,12 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     }
 }
 
-// 2-D view [rows, 128] of a bf16 KV cache; 64 x 64 boxes, 128-byte swizzle.
-bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
+// 2-D view [rows, d] of a bf16 KV cache; 64 x 64 boxes, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 2};
     cuuint32_t box[2] = {64, (cuuint32_t)kKeys};
     cuuint32_t estr[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
@@ -548,7 +561,7 @@ bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows) {
 }  // namespace
 
 bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
-    if (dtype != 1 || p.d != kD) return false;
+    if (dtype != 1 || (p.d != 64 && p.d != 128)) return false;
     if (p.R < 1 || p.R > 512) return false;      // up to four 128-row blocks
     if ((int64_t)p.B * p.Hkv * p.cap >= ((int64_t)1 << 31)) return false;
     return tensor_map_encoder() != nullptr;
@@ -556,17 +569,17 @@ bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
 
 namespace {
 
-template <int ROWS>
+template <int ROWS, int D>
 cudaError_t launch_rows(const CUtensorMap& tmK, const CUtensorMap& tmV, const AttnParams& p,
                         cudaStream_t st) {
-    auto kern = attn_prefix_tc_kernel<ROWS>;
+    auto kern = attn_prefix_tc_kernel<ROWS, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Plan<ROWS>::kSmemBytes);
+                                         Plan<ROWS, D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.S * ((p.R + 127) / 128), p.Hkv, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Plan<ROWS>::kSmemBytes;
+    cfg.dynamicSmemBytes = Plan<ROWS, D>::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -581,9 +594,11 @@ cudaError_t launch_rows(const CUtensorMap& tmK, const CUtensorMap& tmV, const At
 cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
     CUtensorMap tmK, tmV;
     const uint64_t rows = (uint64_t)p.B * p.Hkv * p.cap;
-    if (!make_kv_map(&tmK, p.K, rows) || !make_kv_map(&tmV, p.V, rows))
+    if (!make_kv_map(&tmK, p.K, rows, p.d) || !make_kv_map(&tmV, p.V, rows, p.d))
         return cudaErrorInvalidValue;
-    return p.R <= 64 ? launch_rows<64>(tmK, tmV, p, st) : launch_rows<128>(tmK, tmV, p, st);
+    if (p.d == 64)
+        return p.R <= 64 ? launch_rows<64, 64>(tmK, tmV, p, st) : launch_rows<128, 64>(tmK, tmV, p, st);
+    return p.R <= 64 ? launch_rows<64, 128>(tmK, tmV, p, st) : launch_rows<128, 128>(tmK, tmV, p, st);
 }
 
 }  // namespace rapid

@@ -87,8 +87,13 @@ LLAMA8B_DECODE_120K = Workload("llama3.1-8b_decode_32layers_120k", B=1, Hq=32, H
                                z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0,
                                seed=1007)
 
+# head dimension 64 (a Llama-3.2-1B-shaped target: 32 query / 8 KV heads, 16 layers)
+LLAMA1B_D64_120K = Workload("llama3.2-1b_d64_16layers_120k", B=1, Hq=32, Hkv=8, d=64, n_q=11,
+                            prefix=122880, layers=16, V=128256, dtype="bf16", z_std=3.0,
+                            q_noise_std=1.5, q_noise_uses_T=True, T=1.0, eta=1.0, seed=1008)
+
 ALL = [TINY, LLAMA8B_LAYER_32K, LLAMA8B_120K, LLAMA8B_1LAYER_120K, LLAMA70B_128K, QWEN7B_TREE,
-       QWEN7B_TREE_1LAYER, LLAMA8B_DECODE_120K]
+       QWEN7B_TREE_1LAYER, LLAMA8B_DECODE_120K, LLAMA1B_D64_120K]
 
 
 def gen(seed: int, device="cpu") -> torch.Generator:

@@ -75,22 +75,34 @@ def test_prefix_fills_capacity():
     _run_and_check(w, capacity=1024)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("G,n_q", [(1, 1), (4, 1), (1, 64), (8, 11), (7, 32), (16, 5)])
-def test_group_widths(G, n_q):
-    w = wl.Workload("t", B=1, Hq=2 * G, Hkv=2, d=128, n_q=n_q, prefix=900, layers=1, V=10,
+def test_group_widths(G, n_q, d):
+    w = wl.Workload("t", B=1, Hq=2 * G, Hkv=2, d=d, n_q=n_q, prefix=900, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=40 + G)
     _run_and_check(w)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False)])
-def test_pair_widths_ragged(G, n_q, tree):
-    # 129..256 group rows run on CTA pairs (each CTA loads half of every K/V
-    # tile); ragged prefixes include an empty history and a single key
-    w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=128, n_q=n_q, prefix=2100, layers=1, V=10,
+def test_pair_widths_ragged(G, n_q, tree, d):
+    # 129..256 group rows run as two 128-row-block CTAs that stream the same
+    # K/V tiles; ragged prefixes include an empty history and a single key
+    w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=d, n_q=n_q, prefix=2100, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, tree=tree,
                     tree_nodes_max_depth=6, seed=60 + G + n_q)
     _run_and_check(w, prefix_override=[0, 1, 2100])
     _run_and_check(w, prefix_override=[63, 1000, 65])
+
+
+def test_d64_bf16_long_ragged_history():
+    # head dimension 64 on the tensor-core kernel (one 64-column block of Q,
+    # K and V), 8 KV heads, long ragged histories
+    w = wl.Workload("t", B=3, Hq=32, Hkv=8, d=64, n_q=11, prefix=20000, prefix_lo=3000,
+                    layers=1, V=10, dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True,
+                    seed=81)
+    _run_and_check(w)
+    _run_and_check(w, needle=True)
 
 
 def test_decode_single_query_ragged():

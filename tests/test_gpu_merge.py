@@ -74,18 +74,17 @@ def _shard_caches(K, V, P, n_q, cuts):
     return out
 
 
-@pytest.mark.parametrize("case", ["bf16_d128_chain", "bf16_d128_tree_wide", "f32_d64_chain"])
+@pytest.mark.parametrize("case", ["bf16_d128_chain", "bf16_d128_tree_wide", "bf16_d64_chain",
+                                  "f32_d64_chain"])
 def test_key_shards_merge_to_unsplit_attention(case):
-    if case.startswith("bf16"):
-        dtype, d = torch.bfloat16, 128
-    else:
-        dtype, d = torch.float32, 64
+    dtype = torch.bfloat16 if case.startswith("bf16") else torch.float32
+    d = 128 if "d128" in case else 64
     tree = "tree" in case
     B, Hkv = 2, 2
     G, n_q = (4, 20) if "wide" in case else (4, 6)   # 80 or 24 group rows
     Hq, cap = G * Hkv, 3000
     g = torch.Generator().manual_seed({"bf16_d128_chain": 11, "bf16_d128_tree_wide": 12,
-                                       "f32_d64_chain": 13}[case])
+                                       "bf16_d64_chain": 14, "f32_d64_chain": 13}[case])
     Q = torch.randn((B, Hq, n_q, d), generator=g).to(dtype)
     K = torch.randn((B, Hkv, cap, d), generator=g).to(dtype)
     V = torch.randn((B, Hkv, cap, d), generator=g).to(dtype)
@@ -120,7 +119,8 @@ def test_key_shards_merge_to_unsplit_attention(case):
     assert rapid.rapid_device_error(True) == 0
 
 
-@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64),
+                                     (torch.float32, 64)])
 def test_query_that_sees_no_key(dtype, d):
     # empty history and mask rows that hide every speculative row from some
     # queries: those get O = 0 and LSE = -inf; the other rows match the oracle
