@@ -78,6 +78,18 @@ def test_tree_qwen_vocab():
         _run(w, 1.0, 1.0, 77 + seed, inp=inp)
 
 
+@pytest.mark.parametrize("T,eta,clamp", [(0.6, 5.0, True), (1.0, 0.0, True), (1.3, 1.0, False)])
+def test_tree_temperatures_and_strengths(T, eta, clamp):
+    # the tree rule with a sharper and a flatter target, no knowledge transfer
+    # (eta = 0: p_hat is p), a strong one, and the tail rule off
+    w = wl.Workload("tree", B=4, Hq=1, Hkv=1, d=64, n_q=24, prefix=1, layers=1, V=50021,
+                    dtype="f32", z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, tree=True,
+                    tree_nodes_max_depth=5, seed=9)
+    inp = wl.accept_inputs(w, T=T)
+    for seed in range(3):
+        _run(w, T, eta, 300 + seed, clamp=clamp, inp=inp)
+
+
 def test_small_tree_many_seeds():
     w = wl.Workload("tree", B=6, Hq=1, Hkv=1, d=64, n_q=20, prefix=1, layers=1, V=3001,
                     dtype="f32", z_std=1.5, q_noise_std=0.7, q_noise_uses_T=True, tree=True,

@@ -126,6 +126,13 @@ def test_more_sequences_than_slots(B, Hkv, prefix, tree):
     assert 0 < ws < 64 << 20   # linear in B, not quadratic
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_custom_scale_bf16_tensor_core_path(d):
+    w = wl.Workload("t", B=2, Hq=8, Hkv=2, d=d, n_q=6, prefix=3000, prefix_lo=100, layers=1,
+                    V=10, dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=52 + d)
+    _run_and_check(w, scale=0.2)
+
+
 def test_custom_scale_and_fp32_d128():
     w = wl.Workload("t", B=2, Hq=6, Hkv=3, d=128, n_q=4, prefix=700, prefix_lo=650, layers=1,
                     V=10, dtype="f32", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=51)
