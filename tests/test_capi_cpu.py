@@ -140,3 +140,18 @@ def test_no_cpu_fallback_for_cpu_tensors(lib):
     Q = torch.zeros((1, 4, 5, 128), dtype=torch.bfloat16)
     with pytest.raises(rapid.RapidError):
         rapid.verify_attn(Q, Q, Q, torch.zeros(1, dtype=torch.int32))
+
+
+def test_binding_constants_match_the_header():
+    # every RAPID_* constant the Python binding defines has the header's value
+    text = open(os.path.join(ROOT, "include", "rapid.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    header = {}
+    for name, expr in re.findall(r"\b(RAPID_[A-Z0-9_]+)\s*=\s*([^,}\n]+)", text):
+        parts = [int(x.strip().rstrip("u")) for x in expr.split("<<")]   # literals and shifts
+        header[name] = parts[0] << parts[1] if len(parts) == 2 else parts[0]
+    ours = {k: v for k, v in vars(rapid).items() if k.startswith("RAPID_") and isinstance(v, int)}
+    assert ours
+    for k, v in ours.items():
+        assert k in header, k
+        assert header[k] == v, (k, header[k], v)
