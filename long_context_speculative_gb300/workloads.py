@@ -154,11 +154,25 @@ class AttnInputs:
     parents: List[List[int]] = field(default_factory=list)
 
 
+def tile_signs(rows: int, seed: int, tile: int = 64) -> torch.Tensor:
+    """float32 [rows]: +1 or -1 per run of ``tile`` consecutive cache rows, half
+    of the runs of each sign in a seeded random order."""
+    n = (rows + tile - 1) // tile
+    s = torch.ones(n)
+    s[torch.randperm(n, generator=gen(seed))[: n // 2]] = -1.0
+    return s.repeat_interleave(tile)[:rows]
+
+
 def attn_inputs(w: Workload, layer: int = 0, device="cpu", prefix_override=None,
-                needle: bool = False, capacity: Optional[int] = None) -> AttnInputs:
+                needle: bool = False, capacity: Optional[int] = None,
+                v_offset: float = 0.0, needle_gain: float = 4.0) -> AttnInputs:
     """K, V ~ N(0,1); Q ~ N(0,1) * q_scale.  With ``needle`` 16 history rows of
-    every KV head get K = 4 * (mean query direction of the group), so a handful
-    of rows dominate the output."""
+    every KV head get K = needle_gain * (mean query direction of the group), so
+    a handful of rows dominate the output (a gain of 8 keeps them dominant
+    over a 120K-row history).  With ``v_offset`` = c every V row j gets
+    c * s(j) added to all its entries, s(j) = +-1 per 64-row run of the cache
+    (tile_signs): the output then carries about c / (history / 64) of every
+    run, so a run of keys read twice or not at all moves it by that much."""
     seed = w.seed * 1000 + layer
     dt = torch_dtype(w.dtype)
     cap = capacity if capacity is not None else w.capacity
@@ -170,6 +184,8 @@ def attn_inputs(w: Workload, layer: int = 0, device="cpu", prefix_override=None,
     K = torch.randn((w.B, w.Hkv, cap, w.d), generator=gd, device=device, dtype=torch.float32)
     K = K.to(dt)
     V = torch.randn((w.B, w.Hkv, cap, w.d), generator=gd, device=device, dtype=torch.float32)
+    if v_offset:
+        V += (v_offset * tile_signs(cap, seed + 4)).to(device)[None, None, :, None]
     V = V.to(dt)
     gc = gen(seed + 1)
     Q = (torch.randn((w.B, w.Hq, w.n_q, w.d), generator=gc) * w.q_scale).to(dt).to(device)
@@ -194,7 +210,7 @@ def attn_inputs(w: Workload, layer: int = 0, device="cpu", prefix_override=None,
                 qdir = qdir / (qdir.norm() + 1e-6) * (w.d ** 0.5)
                 rows = torch.randint(0, max(P, 1), (16,), generator=gn)
                 if P > 0:
-                    K[b, g_, rows.to(device)] = (4.0 * qdir).to(dt)
+                    K[b, g_, rows.to(device)] = (needle_gain * qdir).to(dt)
     return AttnInputs(Q=Q, K=K, V=V, prefix_len=pl.to(device), mask=mask, parents=parents)
 
 

@@ -139,59 +139,104 @@ def test_custom_scale_and_fp32_d128():
     _run_and_check(w, scale=0.05)
 
 
-def test_llama8b_layer_32k_all_rows():
-    w = wl.LLAMA8B_LAYER_32K
-    _run_and_check(w)
+# Full-size variants.  "plain": Q, K, V ~ N(0, 1), where |O| is only about
+# sqrt(e / history) per entry (0.005 at 120K), below the 2e-2 tolerance, so
+# this variant pins LSE more than O.  "needle": 16 planted keys per KV head
+# with gain 8, so a few rows dominate O even over a 120K history and the
+# running max jumps by far more than the 2^8 lazy-rescale threshold.
+# "tiles": every V row carries +-c by 64-row run (half the runs of each sign),
+# with c = 0.05 x the runs of the longest history: a run of keys dropped or
+# read twice anywhere in a split moves every entry of O by about 0.05, well
+# past the tolerance, while |O| itself stays small.
+VARIANTS = ["plain", "needle", "tiles"]
 
 
-def test_llama8b_120k_layer_sampled_rows():
-    w = wl.LLAMA8B_120K
-    a = wl.attn_inputs(w, device=DEV, layer=3)
-    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+def _variant(variant, history):
+    if variant == "needle":
+        return dict(needle=True, needle_gain=8.0)
+    if variant == "tiles":
+        return dict(v_offset=0.05 * max(1, history // 64))
+    return {}
+
+
+def _sampled_rows(w, seed, per_group=3):
+    """(b, query head, node) rows: per_group of them for every (sequence, KV head)."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            for _ in range(per_group):
+                rows.append((b, g * w.G + int(rng.integers(0, w.G)), int(rng.integers(0, w.n_q))))
+    return np.array(rows, dtype=np.int64)
+
+
+def _check_sampled(a, mask, rows, label):
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, mask)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(0)
-    rows = np.stack([np.zeros(24, int), rng.integers(0, w.Hq, 24), rng.integers(0, w.n_q, 24)], 1)
     Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
-                                     a.prefix_len.cpu().numpy(), rows, dtype=oracle.DTYPE_BF16)
+                                     a.prefix_len.cpu().numpy(), rows,
+                                     mask=None if mask is None else mask.cpu().numpy(),
+                                     dtype=oracle.DTYPE_BF16)
     Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
     Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
-    check_attn(Og, Lg, Oo, Lo)
+    check_attn(Og, Lg, Oo, Lo, label=label)
+    assert rapid.rapid_device_error(True) == 0
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_llama8b_layer_32k_all_rows(variant):
+    w = wl.LLAMA8B_LAYER_32K
+    a = wl.attn_inputs(w, device=DEV, **_variant(variant, w.prefix))
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
+    torch.cuda.synchronize()
+    Oo, Lo = oracle.verify_attn(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
+                                a.prefix_len.cpu().numpy(), None, dtype=oracle.DTYPE_BF16)
+    check_attn(O.float().cpu().numpy(), L.cpu().numpy(), Oo, Lo, label=f"{w.name} {variant}")
+    assert rapid.rapid_device_error(True) == 0
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_llama8b_120k_layer_sampled_rows(variant):
+    w = wl.LLAMA8B_120K
+    a = wl.attn_inputs(w, device=DEV, layer=3, **_variant(variant, w.prefix))
+    _check_sampled(a, None, _sampled_rows(w, 0), f"{w.name} layer 3 {variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", ["llama70b_128k", "llama8b_decode_120k"])
-def test_other_full_size_shapes_sampled_rows(name):
+def test_other_full_size_shapes_sampled_rows(name, variant):
     # one layer of the 64/8-head 128K shape (88 group rows: the 128-row
     # configuration) and of the single-query decode shape (4 group rows)
     w = {"llama70b_128k": wl.LLAMA70B_128K, "llama8b_decode_120k": wl.LLAMA8B_DECODE_120K}[name]
-    a = wl.attn_inputs(w, device=DEV, layer=1)
-    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
-    torch.cuda.synchronize()
-    rng = np.random.default_rng(2)
-    n = 24
-    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n), rng.integers(0, w.n_q, n)], 1)
-    Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
-                                     a.prefix_len.cpu().numpy(), rows, dtype=oracle.DTYPE_BF16)
-    Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
-    Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
-    check_attn(Og, Lg, Oo, Lo)
+    a = wl.attn_inputs(w, device=DEV, layer=1, **_variant(variant, w.prefix))
+    _check_sampled(a, None, _sampled_rows(w, 2), f"{w.name} layer 1 {variant}")
     del a
     torch.cuda.empty_cache()
 
 
-def test_qwen_tree_shape_sampled_rows():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_qwen_tree_shape_sampled_rows(variant):
+    # 224 group rows: two 128-row-block CTAs per split; four ragged histories
     w = wl.QWEN7B_TREE
-    a = wl.attn_inputs(w, device=DEV, layer=0)
-    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, a.mask)
+    a = wl.attn_inputs(w, device=DEV, layer=0, **_variant(variant, w.prefix))
+    _check_sampled(a, a.mask, _sampled_rows(w, 1), f"{w.name} layer 0 {variant}")
+
+
+@pytest.mark.parametrize("variant", ["needle", "tiles"])
+def test_d128_ragged_20k_60k_all_rows(variant):
+    # three sequences of 20K..60K history rows in one call: the balanced split
+    # plan gives them different split counts, every split a long run of tiles
+    w = wl.Workload("t", B=3, Hq=32, Hkv=8, d=128, n_q=11, prefix=60000, prefix_lo=20000,
+                    layers=1, V=10, dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True,
+                    seed=83)
+    a = wl.attn_inputs(w, device=DEV, **_variant(variant, w.prefix))
+    O, L = rapid.verify_attn(a.Q, a.K, a.V, a.prefix_len, None)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(1)
-    n = 32
-    rows = np.stack([rng.integers(0, w.B, n), rng.integers(0, w.Hq, n), rng.integers(0, w.n_q, n)], 1)
-    Oo, Lo = oracle.verify_attn_rows(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
-                                     a.prefix_len.cpu().numpy(), rows, mask=a.mask.cpu().numpy(),
-                                     dtype=oracle.DTYPE_BF16)
-    Og = O.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
-    Lg = L.cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
-    check_attn(Og, Lg, Oo, Lo)
+    Oo, Lo = oracle.verify_attn(wl.bf16_bits(a.Q), wl.bf16_bits(a.K), wl.bf16_bits(a.V),
+                                a.prefix_len.cpu().numpy(), None, dtype=oracle.DTYPE_BF16)
+    check_attn(O.float().cpu().numpy(), L.cpu().numpy(), Oo, Lo,
+               label=f"ragged 20K-60K d=128 {variant}")
+    assert rapid.rapid_device_error(True) == 0
 
 
 def test_same_result_twice_and_no_kv_writes():
