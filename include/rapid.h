@@ -55,9 +55,13 @@
  *    synchronises the device; results are valid once the stream reaches them.
  *  - Argument checks that need only host-visible values run before any launch
  *    and return RAPID_EINVAL.  Values that live in device memory (prefix
- *    lengths, masks, token ids, parent pointers) are clamped by the kernels to
- *    keep every memory access in bounds; an out-of-range device value gives
- *    unspecified (but memory-safe) results.
+ *    lengths, token ids, parent pointers, node counts) cannot be checked
+ *    without synchronising, so the kernels check them as they run: an
+ *    out-of-range value is clamped (or, for a token id, treated as rejected)
+ *    so that every memory access stays in bounds, the results of that call are
+ *    unspecified, and bit 1 of the device error word is set.
+ *    rapid_stream_status turns that bit into RAPID_EINVAL, and a bounded wait
+ *    that gave up (bit 0) into RAPID_ETIMEOUT.
  *  - No C++ exception crosses this ABI.  Calls are stateless and may be issued
  *    from several host threads on different streams.
  *  - Every per-step quantity that changes between verify steps (history
@@ -78,10 +82,13 @@ extern "C" {
 
 typedef enum {
     RAPID_OK = 0,
-    RAPID_EINVAL = -1,      /* bad argument (host-checkable)                 */
+    RAPID_EINVAL = -1,      /* bad argument (host-checkable), or, from
+                               rapid_stream_status, a bad device-side input */
     RAPID_ECUDA = -2,       /* a CUDA runtime call or kernel launch failed   */
     RAPID_ENOMEM = -3,      /* workspace smaller than the *_workspace_size   */
-    RAPID_EUNSUPPORTED = -4 /* shape outside the compiled kernels' limits    */
+    RAPID_ETIMEOUT = -4,    /* a bounded wait inside a kernel gave up (from
+                               rapid_stream_status): outputs are invalid     */
+    RAPID_EUNSUPPORTED = -5 /* shape outside the compiled kernels' limits    */
 } rapid_status;
 
 /* Element types of Q, K, V and O. */
@@ -125,7 +132,8 @@ size_t rapid_verify_attn_workspace_size(int B, int Hq, int Hkv, int d, int n_q,
  *  prefix_len device int32 [B]: history rows of sequence b are
  *             [0, prefix_len[b]); its n_q speculative rows are
  *             [prefix_len[b], prefix_len[b] + n_q).  Needs
- *             0 <= prefix_len[b] <= kv_capacity - n_q.
+ *             0 <= prefix_len[b] <= kv_capacity - n_q (else the kernels clamp
+ *             it and set bit 1 of the device error word).
  *  spec_mask  device uint8 [B, n_q, n_q] or NULL.  Query i of sequence b sees
  *             speculative row j iff spec_mask[b][i][j] != 0 (a token tree's
  *             ancestor-or-self mask).  NULL means the causal chain j <= i.
@@ -203,7 +211,9 @@ size_t rapid_accept_workspace_size(int B, int n_q, int V);
  *  draft_tokens device int32 [B, n_q]: token of node i (entry 0 unused).
  *  parent       device int32 [B, n_q] or NULL.  NULL = chain (parent of node
  *               i is i-1).  Otherwise parent[b][i] in [0, i) for i >= 1 gives
- *               a token tree; entry 0 is unused.
+ *               a token tree; entry 0 is unused.  A parent outside [0, i) is
+ *               clamped into it and a draft token outside [0, V) counts as
+ *               rejected; both set bit 1 of the device error word.
  *  T            temperature > 0; eta >= 0 and finite (knowledge-transfer
  *               strength of the retrieval-augmented target).
  *  philox_seed  key of the Philox4x32-10 stream.  Node i of sequence b uses
@@ -296,9 +306,11 @@ enum { RAPID_NOALLOC_MAX_NODES = 4096 };
  * held by every GPU that loads the library until the process exits.  It fits
  * B * n_q <= RAPID_NOALLOC_MAX_NODES; larger sizes return RAPID_EUNSUPPORTED.
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
- * routine).  Its first call on a device looks up the array's device address
- * with cudaGetSymbolAddress while that device is current; make that first
- * call before any stream capture.
+ * routine).  Every call looks up the array's device address on the current
+ * device with cudaGetSymbolAddress (which allocates nothing), so a reset
+ * device or a re-created context never sees a stale address.  The first
+ * lookup on a device may load the library's device code there: make the
+ * first call on a device before any stream capture.
  *
  * Concurrency: every call on a device shares the one array, and the array
  * keeps the last call's contents.  Calls whose kernels overlap on the GPU
@@ -306,8 +318,9 @@ enum { RAPID_NOALLOC_MAX_NODES = 4096 };
  * them) race on it and give wrong results; order such calls, for example on
  * one stream.
  *
- * Errors: those of rapid_accept, plus RAPID_EUNSUPPORTED for B * n_q over the
- * limit and RAPID_ECUDA when the array's address cannot be obtained.
+ * Errors: those of rapid_accept (RAPID_EINVAL for B < 1 or n_q outside
+ * [1, RAPID_MAX_NQ], among others), plus RAPID_EUNSUPPORTED for B * n_q over
+ * the limit and RAPID_ECUDA when the array's address cannot be obtained.
  */
 rapid_status rapid_accept_noalloc(const float* z_target, const float* q_draft,
                                   const int32_t* draft_tokens, const int32_t* parent,
@@ -328,13 +341,40 @@ int rapid_version(void);
 
 /*
  * Sticky error bits that kernels of this library raised on the CURRENT device
- * (bit 0: a bounded wait for an asynchronous copy gave up, so the outputs of
- * that call are invalid; bit 1: rapid_kv_commit, rapid_kv_advance or
- * rapid_retrieval_select found an invalid device-side input and left that
- * sequence alone).  Synchronises the device to read the word; clears it
- * when `clear` is non-zero.  Returns -1 if the word could not be read.
+ * (bit 0: a bounded wait for an asynchronous copy or a peer gave up, so the
+ * outputs of that call are invalid; bit 1: a kernel found an invalid
+ * device-side input -- a history length, parent, draft token or node count
+ * out of range in rapid_verify_attn / rapid_accept*, or an input that
+ * rapid_kv_commit, rapid_kv_advance or rapid_retrieval_select refused,
+ * leaving that sequence alone).  Synchronises the device to read the word;
+ * clears it when `clear` is non-zero.  Returns -1 if the word could not be
+ * read.
  */
 int rapid_device_error(int clear);
+
+/*
+ * The status of the work issued so far: synchronises `stream`, then reads the
+ * sticky error word of the current device (the word is per device, not per
+ * stream) and clears it when `clear` is non-zero.  Returns RAPID_ETIMEOUT if
+ * a bounded wait inside a kernel gave up (the outputs of that call are
+ * invalid), else RAPID_EINVAL if a kernel found an out-of-range device-side
+ * input, else RAPID_OK; RAPID_ECUDA if the synchronisation or the read
+ * failed (a sticky CUDA error, for instance).
+ */
+rapid_status rapid_stream_status(void* stream, int clear);
+
+/*
+ * Self-test of the bounded waits that every kernel of this library uses on
+ * its mbarriers: one small kernel starts a bulk copy, then waits on a barrier
+ * phase that nothing completes.  After `limit_ns` nanoseconds (clamped to
+ * [1000, 1e9]) the wait gives up, records bit 0 and the code 0xC7000001 in
+ * the device error record (rapid_device_error_info), waits for its copy to
+ * land and returns, exactly as a kernel whose producer stalled would.  A
+ * following rapid_stream_status returns RAPID_ETIMEOUT.  The library has no
+ * other way to make a wait run out on purpose; no fault is involved.
+ * Errors: RAPID_ECUDA when the launch fails.
+ */
+rapid_status rapid_wait_selftest(uint64_t limit_ns, void* stream);
 
 /*
  * The full error record of the current device: words8[0] = the sticky bits of

@@ -614,6 +614,27 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     const int n_q = p.n_q;
     griddep_wait();
     const int nn = node_count(p, b);   // nodes of this sequence
+    // Device-side inputs the host cannot check (clamped or rejected on the
+    // way, so memory stays safe): a node count outside [1, n_q], a parent
+    // outside [0, i) or a draft token outside the vocabulary sets the
+    // bad-input bit of the error word (one CTA of the cluster looks).
+    if (cs == 0 && t < n_q && p.err) {
+        bool bad = false;
+        if (t == 0) {
+            if (p.n_nodes) {
+                const int c = p.n_nodes[b];
+                bad = c < 1 || c > n_q;
+            }
+        } else if (t < nn) {
+            const int tok = p.tokens[(int64_t)b * n_q + t];
+            bad = tok < 0 || tok >= p.V;
+            if (p.parent) {
+                const int par = p.parent[(int64_t)b * n_q + t];
+                bad = bad || par < 0 || par >= t;
+            }
+        }
+        if (bad) atomicOr(p.err, kErrBadInput);
+    }
     if (t < n_q) {
         s_acc[t] = t == 0 ? 1 : p.ws_accept[(int64_t)b * n_q + t];
         s_par[t] = t == 0 ? -1 : parent_of(p, b, t);

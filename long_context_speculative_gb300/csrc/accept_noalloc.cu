@@ -11,8 +11,6 @@
 // below, which every GPU that loads librapid.so holds until the process
 // exits.  The verification step of the pages has no counterpart of this; it
 // is a packaging variant of rapid_accept.
-#include <atomic>
-
 #include <cuda_runtime.h>
 
 #include "rapid.h"
@@ -29,25 +27,17 @@ constexpr size_t kScratchBytes = align256(kNodes * sizeof(int32_t)) +
 // Shared by every call on a device; see the concurrency note in rapid.h.
 static __device__ __align__(256) unsigned char g_accept_scratch[kScratchBytes];
 
-// Device address of g_accept_scratch for each device, looked up on the first
-// call made while that device is current.  In host code the name
-// g_accept_scratch is only a host-side stand-in, never a device address.
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
-
+// Device address of g_accept_scratch on the current device.  In host code the
+// name g_accept_scratch is only a host-side stand-in, never a device address.
+// It is looked up on every call (cudaGetSymbolAddress allocates nothing and
+// costs well under a microsecond once the module is loaded), so a device
+// reset or a re-created context never leaves a stale cached address.
 void* scratch_address() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        (void)cudaGetLastError();
-        return nullptr;
-    }
-    void* ptr = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (ptr) return ptr;
+    void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_accept_scratch) != cudaSuccess || ptr == nullptr) {
         (void)cudaGetLastError();
         return nullptr;
     }
-    g_scratch_addr[dev].store(ptr, std::memory_order_release);
     return ptr;
 }
 
@@ -60,7 +50,8 @@ extern "C" rapid_status rapid_accept_noalloc(const float* z_target, const float*
                                              uint64_t philox_seed, uint32_t flags,
                                              int32_t* n_accepted, int32_t* next_token,
                                              int32_t* path, float* diag, void* stream) {
-    if (B < 1 || n_q < 1 || (int64_t)B * n_q > RAPID_NOALLOC_MAX_NODES) return RAPID_EUNSUPPORTED;
+    if (B < 1 || n_q < 1 || n_q > RAPID_MAX_NQ) return RAPID_EINVAL;
+    if ((int64_t)B * n_q > RAPID_NOALLOC_MAX_NODES) return RAPID_EUNSUPPORTED;
     void* scratch = rapid::scratch_address();
     if (!scratch) return RAPID_ECUDA;
     // Nothing in the scratch needs to start at zero: every entry that the

@@ -43,6 +43,7 @@ struct AttnParams {
 };
 
 // History length of sequence b, clamped so every access stays in the cache.
+// (The merge kernel flags an out-of-range value in the device error word.)
 __device__ __forceinline__ int64_t clamped_prefix(const AttnParams& p, int b) {
     int64_t P = p.prefix_len[b];
     if (P < 0) P = 0;
@@ -112,8 +113,9 @@ __device__ __forceinline__ SplitOf split_of(const AttnParams& p, int pairs, int 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_prefix_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
-// tcgen05 + TMA prefix kernel (bf16, d = 128, R <= 128).  Returns
-// cudaErrorNotSupported when the shape is outside what it handles.
+// tcgen05 + TMA prefix kernel (bf16 caches, d = 64 or 128, up to 512 group
+// rows R = G * n_q, run as 128-row blocks).  attn_prefix_tc_supported() says
+// whether a shape is one it handles.
 cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t s);
 bool attn_prefix_tc_supported(const AttnParams& p, int dtype);
 

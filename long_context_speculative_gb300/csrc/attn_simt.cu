@@ -203,6 +203,15 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const AttnPar
     const int g = bg % p.Hkv;
     const int h = g * p.G + r / p.n_q;
     const int i = r % p.n_q;
+    // A device-side input the host cannot check: once per sequence, a history
+    // length outside [0, kv_capacity - n_q] (clamped everywhere) sets the
+    // bad-input bit of the error word.  (A mask row may hide every
+    // speculative row, even the query's own node: a key-range shard of the
+    // history that must not see them passes an all-zero mask.)
+    if (tid == 0 && g == 0 && r == 0 && p.err) {
+        const int64_t P = p.prefix_len[b];
+        if (P < 0 || P > p.cap - p.n_q) atomicOr(p.err, kErrBadInput);
+    }
     // partial slots written for this sequence: all S of (b, g) for the
     // CUDA-core history kernel; the S_b slots from part_first for the
     // tensor-core kernel

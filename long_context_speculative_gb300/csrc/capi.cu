@@ -150,6 +150,28 @@ rapid_status accept_launch(const float* z_target, const float* q_draft,
     return launch_accept(p, sh, st) == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
 }
 
+// Self-test of the bounded waits (rapid_wait_selftest): a copy in flight,
+// then a wait on a phase nothing completes, which must give up, record its
+// code and let the copy land before the CTA leaves.
+constexpr unsigned int kSelftestCode = 0x47000001u;   // recorded as 0xC7000001
+__device__ __align__(16) unsigned char g_selftest_src[1024];
+
+__global__ void wait_selftest_kernel(unsigned int* err, uint64_t limit_ns) {
+    __shared__ __align__(128) unsigned char buf[1024];
+    __shared__ __align__(8) uint64_t copied;
+    __shared__ __align__(8) uint64_t never;
+    if (threadIdx.x == 0) {
+        mbar_init(&copied, 1);
+        mbar_init(&never, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&copied, (uint32_t)sizeof(buf));
+        bulk_g2s(buf, g_selftest_src, (uint32_t)sizeof(buf), &copied);
+        (void)mbar_wait(&never, 0u, err, kSelftestCode, limit_ns);
+        (void)mbar_wait(&copied, 0u, err, kSelftestCode + 1u);
+    }
+    __syncthreads();
+}
+
 bool lm_head_args_ok(int rows, int hidden_dim, int V) {
     if (rows < 1 || rows > RAPID_LM_HEAD_MAX_ROWS) return false;
     if (hidden_dim < 64 || hidden_dim > RAPID_LM_HEAD_MAX_HIDDEN || hidden_dim % 64 != 0) return false;
@@ -370,12 +392,13 @@ const char* rapid_status_string(int status) {
         case RAPID_EINVAL: return "invalid argument";
         case RAPID_ECUDA: return "CUDA error";
         case RAPID_ENOMEM: return "workspace too small";
+        case RAPID_ETIMEOUT: return "a bounded wait inside a kernel gave up";
         case RAPID_EUNSUPPORTED: return "unsupported shape";
         default: return "unknown status";
     }
 }
 
-int rapid_version(void) { return 100; }
+int rapid_version(void) { return 200; }
 
 rapid_status rapid_kv_commit(void* const* K_layers, void* const* V_layers, int layers, int dtype,
                              int B, int Hkv, int d, int64_t kv_capacity, int n_q,
@@ -449,6 +472,27 @@ int rapid_device_error(int clear) {
     uint32_t w[8];
     if (rapid_device_error_info(w, clear) != 0) return -1;
     return (int)w[0];
+}
+
+rapid_status rapid_stream_status(void* stream, int clear) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RAPID_ECUDA;
+    }
+    uint32_t w[8];
+    if (rapid_device_error_info(w, clear) != 0) return RAPID_ECUDA;
+    if (w[0] & kErrWaitTimeout) return RAPID_ETIMEOUT;
+    if (w[0] & kErrBadInput) return RAPID_EINVAL;
+    return RAPID_OK;
+}
+
+rapid_status rapid_wait_selftest(uint64_t limit_ns, void* stream) {
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > kWaitLimitNs) limit_ns = kWaitLimitNs;
+    unsigned int* err = device_error_word();
+    if (!err) return RAPID_ECUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? RAPID_OK : RAPID_ECUDA;
 }
 
 int rapid_device_error_info(uint32_t* words8, int clear) {

@@ -17,6 +17,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "librapid.so")
 
 RAPID_OK = 0
 RAPID_EINVAL = -1
+RAPID_ECUDA = -2
+RAPID_ENOMEM = -3
+RAPID_ETIMEOUT = -4
+RAPID_EUNSUPPORTED = -5
 RAPID_DTYPE_F32 = 0
 RAPID_DTYPE_BF16 = 1
 RAPID_ACCEPT_TAIL_CLAMP = 1
@@ -25,6 +29,7 @@ RAPID_MAX_VOCAB = 229376
 RAPID_COMMIT_MAX_LAYERS = 128
 RAPID_RETRIEVAL_MAX_CHUNKS = 8192
 RAPID_LM_HEAD_MAX_ROWS = 256
+RAPID_NOALLOC_MAX_NODES = 4096
 
 _lib = None
 
@@ -68,6 +73,10 @@ def lib() -> ctypes.CDLL:
     L.rapid_device_error.restype = i32
     L.rapid_device_error_info.argtypes = [vp, i32]
     L.rapid_device_error_info.restype = i32
+    L.rapid_stream_status.argtypes = [vp, i32]
+    L.rapid_stream_status.restype = i32
+    L.rapid_wait_selftest.argtypes = [u64, vp]
+    L.rapid_wait_selftest.restype = i32
     L.rapid_accept_noalloc.argtypes = [vp, vp, vp, vp, i32, i32, i32, f32, f32, u64, u32, vp, vp,
                                        vp, vp, vp]
     L.rapid_accept_noalloc.restype = i32
@@ -114,6 +123,41 @@ def _need_cuda(*ts):
             raise RapidError("librapid works on CUDA tensors only (no CPU path)")
         if t is not None and not t.is_contiguous():
             raise RapidError("librapid needs contiguous tensors")
+
+
+def _need_same_device(*ts):
+    """Every tensor on the current CUDA device (the launches go to it)."""
+    cur = torch.cuda.current_device()
+    for t in ts:
+        if t is not None and t.device.index != cur:
+            raise RapidError(f"tensor on {t.device}, but the current device is cuda:{cur}")
+
+
+def _need(t, dtype, shape, name):
+    if t is not None and (t.dtype != dtype or tuple(t.shape) != tuple(shape)):
+        raise RapidError(f"{name} must be a {dtype} tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
+def _check_accept_tensors(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path,
+                          diag, n_nodes=None):
+    """The sizes the kernels will index by: z and q float32 [B, n_q, V]; tokens,
+    parents and the path int32 [B, n_q]; counts int32 [B]; diag float32 [B, n_q, 5]."""
+    if z_target is None or z_target.dim() != 3:
+        raise RapidError("z_target must be a [B, n_q, V] tensor")
+    B, n_q, V = z_target.shape
+    _need(z_target, torch.float32, (B, n_q, V), "z_target")
+    _need(q_draft, torch.float32, (B, n_q, V), "q_draft")
+    _need(draft_tokens, torch.int32, (B, n_q), "draft_tokens")
+    _need(parent, torch.int32, (B, n_q), "parent")
+    _need(n_accepted, torch.int32, (B,), "n_accepted")
+    _need(next_token, torch.int32, (B,), "next_token")
+    _need(path, torch.int32, (B, n_q), "path")
+    _need(diag, torch.float32, (B, n_q, 5), "diag")
+    _need(n_nodes, torch.int32, (B,), "n_nodes")
+    _need_same_device(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag,
+                      n_nodes)
+    return B, n_q, V
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -168,7 +212,8 @@ def rapid_accept(z_target, q_draft, draft_tokens, parent, T, eta, philox_seed, f
                  n_accepted, next_token, path, diag, workspace, stream=None):
     _need_cuda(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag,
                workspace)
-    B, n_q, V = z_target.shape
+    B, n_q, V = _check_accept_tensors(z_target, q_draft, draft_tokens, parent, n_accepted,
+                                      next_token, path, diag)
     st = lib().rapid_accept(_ptr(z_target), _ptr(q_draft), _ptr(draft_tokens), _ptr(parent), B,
                             n_q, V, float(T), float(eta), int(philox_seed) & ((1 << 64) - 1),
                             int(flags), _ptr(n_accepted), _ptr(next_token), _ptr(path),
@@ -184,9 +229,8 @@ def rapid_accept_ex(z_target, q_draft, draft_tokens, parent, n_nodes, T, eta, ph
     read by the kernels when they run."""
     _need_cuda(z_target, q_draft, draft_tokens, parent, n_nodes, n_accepted, next_token, path,
                diag, workspace)
-    B, n_q, V = z_target.shape
-    if n_nodes is not None and (n_nodes.dtype != torch.int32 or n_nodes.numel() != B):
-        raise RapidError("n_nodes must be an int32 tensor of B entries")
+    B, n_q, V = _check_accept_tensors(z_target, q_draft, draft_tokens, parent, n_accepted,
+                                      next_token, path, diag, n_nodes)
     if isinstance(philox_seed, torch.Tensor):
         _need_cuda(philox_seed)
         if philox_seed.dtype not in (torch.int64, torch.uint64) or philox_seed.numel() != 1:
@@ -206,7 +250,8 @@ def rapid_accept_noalloc(z_target, q_draft, draft_tokens, parent, T, eta, philox
                          n_accepted, next_token, path, diag, stream=None):
     """rapid_accept with the library's static scratch instead of a workspace."""
     _need_cuda(z_target, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag)
-    B, n_q, V = z_target.shape
+    B, n_q, V = _check_accept_tensors(z_target, q_draft, draft_tokens, parent, n_accepted,
+                                      next_token, path, diag)
     st = lib().rapid_accept_noalloc(_ptr(z_target), _ptr(q_draft), _ptr(draft_tokens),
                                     _ptr(parent), B, n_q, V, float(T), float(eta),
                                     int(philox_seed) & ((1 << 64) - 1), int(flags),
@@ -220,6 +265,10 @@ def rapid_lm_head(hidden, W_lm, z, stream=None):
     _need_cuda(hidden, W_lm, z)
     rows, hd = hidden.shape
     V = W_lm.shape[0]
+    _need(hidden, torch.bfloat16, (rows, hd), "hidden")
+    _need(W_lm, torch.bfloat16, (V, hd), "W_lm")
+    _need(z, torch.float32, (rows, V), "z")
+    _need_same_device(hidden, W_lm, z)
     st = lib().rapid_lm_head(_ptr(hidden), _ptr(W_lm), rows, hd, V, _ptr(z), _stream(stream))
     _check(st, "rapid_lm_head")
 
@@ -233,7 +282,11 @@ def rapid_lm_head_accept(hidden, W_lm, q_draft, draft_tokens, parent, T, eta, ph
     """rapid_accept on the logits of hidden [B*n_q, hidden_dim] against W_lm [V, hidden_dim]."""
     _need_cuda(hidden, W_lm, q_draft, draft_tokens, parent, n_accepted, next_token, path, diag,
                workspace)
-    B, n_q, V = q_draft.shape
+    B, n_q, V = _check_accept_tensors(q_draft, q_draft, draft_tokens, parent, n_accepted,
+                                      next_token, path, diag)
+    _need(hidden, torch.bfloat16, (B * n_q, hidden.shape[-1]), "hidden")
+    _need(W_lm, torch.bfloat16, (V, hidden.shape[-1]), "W_lm")
+    _need_same_device(hidden, W_lm, workspace)
     st = lib().rapid_lm_head_accept(_ptr(hidden), _ptr(W_lm), hidden.shape[1], _ptr(q_draft),
                                     _ptr(draft_tokens), _ptr(parent), B, n_q, V, float(T),
                                     float(eta), int(philox_seed) & ((1 << 64) - 1), int(flags),
@@ -250,9 +303,11 @@ def rapid_lm_head_accept_ex(hidden, W_lm, q_draft, draft_tokens, parent, n_nodes
     (philox_seed: an int, or a one-element 64-bit integer CUDA tensor)."""
     _need_cuda(hidden, W_lm, q_draft, draft_tokens, parent, n_nodes, n_accepted, next_token,
                path, diag, workspace)
-    B, n_q, V = q_draft.shape
-    if n_nodes is not None and (n_nodes.dtype != torch.int32 or n_nodes.numel() != B):
-        raise RapidError("n_nodes must be an int32 tensor of B entries")
+    B, n_q, V = _check_accept_tensors(q_draft, q_draft, draft_tokens, parent, n_accepted,
+                                      next_token, path, diag, n_nodes)
+    _need(hidden, torch.bfloat16, (B * n_q, hidden.shape[-1]), "hidden")
+    _need(W_lm, torch.bfloat16, (V, hidden.shape[-1]), "W_lm")
+    _need_same_device(hidden, W_lm, workspace)
     if isinstance(philox_seed, torch.Tensor):
         _need_cuda(philox_seed)
         if philox_seed.dtype not in (torch.int64, torch.uint64) or philox_seed.numel() != 1:
@@ -349,6 +404,17 @@ def rapid_device_error_info(clear: bool = True):
     if lib().rapid_device_error_info(ctypes.cast(words, ctypes.c_void_p), 1 if clear else 0) != 0:
         raise RapidError("could not read the device error record")
     return list(words)
+
+
+def rapid_stream_status(stream=None, clear: bool = True) -> int:
+    """Synchronise the stream and return RAPID_OK, RAPID_ETIMEOUT (a bounded wait
+    inside a kernel gave up), RAPID_EINVAL (a bad device-side input) or RAPID_ECUDA."""
+    return int(lib().rapid_stream_status(_stream(stream), 1 if clear else 0))
+
+
+def rapid_wait_selftest(limit_ns: int, stream=None):
+    """Launch the bounded-wait self-test kernel (its wait gives up after limit_ns)."""
+    _check(lib().rapid_wait_selftest(int(limit_ns), _stream(stream)), "rapid_wait_selftest")
 
 
 def rapid_version() -> int:

@@ -69,4 +69,31 @@ def test_noalloc_rejects_sizes_over_the_limit():
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     st = L.rapid_accept_noalloc(p(z), p(z), p(tok), None, B, n_q, V, 1.0, 1.0, 0, 1, p(o), p(o),
                                 None, None, None)
-    assert st == -4   # RAPID_EUNSUPPORTED
+    assert st == rapid.RAPID_EUNSUPPORTED
+    # sizes that no entry point accepts are invalid arguments, as for rapid_accept
+    for b, n in ((0, 11), (1, 0), (1, 65)):
+        st = L.rapid_accept_noalloc(p(z), p(z), p(tok), None, b, n, V, 1.0, 1.0, 0, 1, p(o),
+                                    p(o), None, None, None)
+        assert st == rapid.RAPID_EINVAL, (b, n)
+
+
+def test_noalloc_allocates_nothing():
+    # after a first call (which may load the library's device code), further
+    # calls leave the device's free memory exactly where it was
+    w = wl.Workload("noalloc_mem", B=2, Hq=1, Hkv=1, d=64, n_q=11, prefix=1, layers=1, V=32000,
+                    dtype="f32", z_std=3.0, q_noise_std=1.5, q_noise_uses_T=True, seed=73)
+    inp = wl.accept_inputs(w)
+    z, q, tok = inp.z.to(DEV), inp.q.to(DEV), inp.tokens.to(DEV)
+    n_acc, nxt, path, diag = _outputs(w.B, w.n_q)
+    call = lambda s: rapid.rapid_accept_noalloc(z, q, tok, None, 1.0, 1.0, s,
+                                                rapid.RAPID_ACCEPT_TAIL_CLAMP, n_acc, nxt, path,
+                                                diag)
+    call(0)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for s in range(50):
+        call(s)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert rapid.rapid_device_error(True) == 0
