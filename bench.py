@@ -26,6 +26,7 @@ sys.path.insert(0, ROOT)
 METRIC = "verify-step KV-cache HBM GB/s vs GB300 peak; verify steps/s at 120K context"
 UNIT = "verify_steps/s"
 WORKLOAD = "llama3.1-8b_32layers_120k"
+WORKLOAD_DEFAULT = WORKLOAD
 # The traffic record is one 120K Llama-3.1-8B-shaped layer: the per-launch shape
 # of these workloads.
 TRAFFIC_WORKLOADS = ("llama3.1-8b_32layers_120k", "llama3.1-8b_1layer_120k")
@@ -60,15 +61,96 @@ def _dist_env():
     return ws, rank, local
 
 
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal (about 8 TB/s)
+
+# NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+_NVML_REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x4: "sw_power_cap"}
+
+
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, the
+    driver's own library, through ctypes) every `period_s` in a thread: fine
+    enough to sample a timed region of a few tens of milliseconds."""
+
+    def __init__(self, dev_index: int, period_s: float = 0.005):
+        import ctypes
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            found = False
+            try:
+                import torch
+                uuid = str(torch.cuda.get_device_properties(dev_index).uuid)
+                if not uuid.startswith("GPU-"):
+                    uuid = "GPU-" + uuid
+                found = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                found = False
+            if not found and nv.nvmlDeviceGetHandleByIndex_v2(dev_index, ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h, self.ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        ct = self.ct
+        mhz = ct.c_uint()
+        reasons = ct.c_ulonglong()
+        while not self.stop:
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0 and \
+                    self.reasons_fn(self.h, ct.byref(reasons)) == 0:
+                self.samples.append((float(mhz.value), int(reasons.value)))
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.stop = False
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self.stop = True
+            self.t.join(timeout=2)
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        sm = sorted(x for x, _ in self.samples)
+        reasons = set()
+        for _, bits in self.samples:
+            for bit, name in _NVML_REASONS.items():
+                if bits & bit:
+                    reasons.add(name)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(sm), "source": f"NVML every {self.period * 1e3:.0f} ms"}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled during the timed region,
+    with NVML sampled every 5 ms beside it (a timed region of a few tens of
+    milliseconds gets only one or two nvidia-smi samples)."""
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.nvml = NvmlClocks(gpu_index)
 
     def __enter__(self):
+        self.nvml.__enter__()
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -88,6 +170,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def __exit__(self, *a):
+        self.nvml.__exit__()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -96,6 +179,17 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        nv = self.nvml.summary()
+        smi = self.smi_summary()
+        if nv is None:
+            return smi
+        # NVML's many samples decide the median; reasons seen by either count
+        nv["reasons"] = sorted(set(nv["reasons"]) | set(r for r in smi["reasons"]
+                                                       if r != "unavailable"))
+        nv["nvidia_smi_samples"] = smi["samples"]
+        return nv
+
+    def smi_summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -360,6 +454,9 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e_start.elapsed_time(e_end), dev)
 
+    # ---- rapid_accept alone on this step's own inputs (its share of a step) --
+    acc_step_ms = accept_alone_ms(z, q, tok, par, w, ws_acc, n_acc, nxt, stream)
+
     # ---- acceptance bandwidth on batches larger than L2 ----------------------
     acc_roof = accept_batch_roofline(w, dev, stream)
     # and on the tree configuration's own step (4 x 32 rows of 152064 entries)
@@ -384,13 +481,16 @@ def run_gpu(args, w):
     ms_per_step = total_ms / args.steps
     value = whole_job_rate(ws, args.steps, total_ms)
     e2e_value = whole_job_rate(ws, args.steps, e2e_ms)
-    kv_rows = int(prefix_len.sum().item()) + w.B * w.n_q
-    kv_bytes = 2 * w.Hkv * kv_rows * w.d * 2
-    qo_bytes = 2 * w.B * w.Hq * w.n_q * w.d * 2 + w.B * w.Hq * w.n_q * 4
-    per_call = kv_bytes + qo_bytes
+    per_call = attn_call_bytes(w, prefix_len)
     attn_ms.sort()
     avg_call_ms = sum(attn_ms) / len(attn_ms)
-    achieved = per_call / (avg_call_ms * 1e-3) / 1e9
+    # The calls of the timed region run back to back, so the average call is
+    # the step time less the acceptance's own share, over the layers.  The
+    # event-bracketed pass after it keeps calls from overlapping and reads a
+    # little slower; both are reported.
+    step_call_ms = (ms_per_step - acc_step_ms) / w.layers
+    achieved = per_call / (step_call_ms * 1e-3) / 1e9
+    achieved_ev = per_call / (avg_call_ms * 1e-3) / 1e9
     peak, peak_src = _peaks()
     step_gbs = (per_call * w.layers + 2 * w.B * w.n_q * w.V * 4) / (ms_per_step * 1e-3) / 1e9
     launches_per_step = 2 * w.layers + 2
@@ -409,13 +509,23 @@ def run_gpu(args, w):
             "kv_hbm_gbs_step": step_gbs,
             "roofline": {"bound": "hbm", "kernel": "rapid_verify_attn (history + merge kernels)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs, copy)",
+                         "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                         "peak_source": peak_src + " (hbm_gbs, copy)",
+                         "nominal_peak": NOMINAL_HBM_GBS,
                          "traffic": (_traffic_for("verify_attn_llama8b_120k")
                                      if w.name in TRAFFIC_WORKLOADS else None),
                          "algorithmic_bytes_per_launch": per_call,
-                         "avg_launch_ms": avg_call_ms,
-                         "timing": f"CUDA events around every call, {roof_steps} steps after "
-                                   "the timed region"},
+                         "avg_launch_ms": step_call_ms,
+                         "timing": (f"timed region: (ms_per_step {ms_per_step:.4f} - rapid_accept "
+                                    f"alone on the step's inputs {acc_step_ms:.4f}) / "
+                                    f"{w.layers} layers"),
+                         "per_call_events": {
+                             "avg_launch_ms": avg_call_ms, "achieved": achieved_ev,
+                             "frac": achieved_ev / peak,
+                             "frac_nominal": achieved_ev / NOMINAL_HBM_GBS,
+                             "timing": f"CUDA events around every call, {roof_steps} steps "
+                                       "after the timed region (calls cannot overlap)"}},
+            "accept_step_ms": acc_step_ms,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "accept_roofline": acc_roof,
@@ -428,15 +538,167 @@ def run_gpu(args, w):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
             "wall_s_timed": wall}
+    # ---- the other workloads of the step, each timed the same way ----------
+    del Ks, Vs, Qs, O_all, L_all, Os, Ls, dQ, hQ, hO, hL
+    torch.cuda.empty_cache()
+    if not args.no_extras and w.name == WORKLOAD_DEFAULT:
+        line["extras"] = {x.name: extra_workload(x, dev, stream)
+                          for x in (wl.LLAMA70B_128K, wl.QWEN7B_TREE, wl.LLAMA8B_DECODE_120K,
+                                    wl.LLAMA1B_D64_120K)}
     if rank == 0 and not args.no_cpu_baseline:
         t, cores, sample, _ = oracle_sample_time(w, layers_sample=3, groups_sample=w.Hkv)
         line["cpu_baseline"] = {"value": 1.0 / t, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
+        # the same oracle run on the bench's acceptance inputs: decisions and
+        # tokens of the CUDA path against it, near-boundary cases counted
+        line["parity_exemptions"] = parity_exemptions(w, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def attn_call_bytes(w, prefix_len):
+    """Algorithmic bytes of one rapid_verify_attn call: K and V of the history
+    and speculative rows read once per KV head, Q read, O and LSE written."""
+    kv_rows = int(prefix_len.sum().item()) + w.B * w.n_q
+    kv_bytes = 2 * w.Hkv * kv_rows * w.d * 2
+    qo_bytes = 2 * w.B * w.Hq * w.n_q * w.d * 2 + w.B * w.Hq * w.n_q * 4
+    return kv_bytes + qo_bytes
+
+
+def accept_alone_ms(z, q, tok, par, w, ws_acc, n_acc, nxt, stream, reps=50):
+    """Device time of one rapid_accept on a step's own inputs, back to back."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+
+    def call(seed):
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                           n_acc, nxt, None, None, ws_acc)
+
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(reps):
+        call(0x5EED2000 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def extra_workload(w, dev, stream, steps=10, warmup=3, roof_steps=5):
+    """One more workload of the verify step, timed as the headline one: `steps`
+    steps back to back (all layers of rapid_verify_attn, then rapid_accept),
+    every call's share from the step time less the acceptance alone, and a
+    pass with events around every call.  The caches exceed L2."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    Ks, Vs, Qs = [], [], []
+    for layer in range(w.layers):
+        a = wl.attn_inputs(w, layer=layer, device=dev)
+        Ks.append(a.K); Vs.append(a.V); Qs.append(a.Q)
+        if layer == 0:
+            mask, prefix_len, parents = a.mask, a.prefix_len, a.parents
+        del a
+    acc_in = wl.accept_inputs(w, parents=parents if w.tree else None)
+    z, q, tok = acc_in.z.to(dev), acc_in.q.to(dev), acc_in.tokens.to(dev)
+    par = None if acc_in.parent is None else acc_in.parent.to(dev)
+    O = torch.empty_like(Qs[0])
+    L = torch.empty((w.B, w.Hq, w.n_q), dtype=torch.float32, device=dev)
+    ws_attn = torch.empty(rapid.rapid_verify_attn_workspace_size(
+        w.B, w.Hq, w.Hkv, w.d, w.n_q, w.capacity, rapid.RAPID_DTYPE_BF16), dtype=torch.uint8,
+        device=dev)
+    ws_acc = torch.empty(rapid.rapid_accept_workspace_size(w.B, w.n_q, w.V), dtype=torch.uint8,
+                         device=dev)
+    n_acc = torch.empty(w.B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(w.B, dtype=torch.int32, device=dev)
+
+    def step(seed, ev=None):
+        for layer in range(w.layers):
+            if ev is not None:
+                ev[layer].record(stream)
+            rapid.rapid_verify_attn(Qs[layer], Ks[layer], Vs[layer], prefix_len, mask, 0.0, O, L,
+                                    ws_attn)
+        if ev is not None:
+            ev[w.layers].record(stream)
+        rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
+                           n_acc, nxt, None, None, ws_acc)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(0x5EED0000 + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(w.layers + 1)]
+           for _ in range(roof_steps)]
+    for i in range(roof_steps):
+        step(0x5EED1000 + i, evs[i])
+    torch.cuda.synchronize()
+    per_ev = [evs[i][l].elapsed_time(evs[i][l + 1]) for i in range(roof_steps)
+              for l in range(w.layers)]
+    acc_ms = accept_alone_ms(z, q, tok, par, w, ws_acc, n_acc, nxt, stream)
+    assert rapid.rapid_device_error(True) == 0
+    per_call = attn_call_bytes(w, prefix_len)
+    peak, _ = _peaks()
+    call_ms = (ms_step - acc_ms) / w.layers
+    ev_ms = sum(per_ev) / len(per_ev)
+    gbs = per_call / (call_ms * 1e-3) / 1e9
+    gbs_ev = per_call / (ev_ms * 1e-3) / 1e9
+    out = {"verify_steps_per_s": 1e3 / ms_step, "ms_per_step": ms_step, "layers": w.layers,
+           "B": w.B, "n_q": w.n_q, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+           "history": [int(x) for x in prefix_len.tolist()],
+           "algorithmic_bytes_per_call": per_call, "accept_ms": acc_ms,
+           "call_ms": call_ms, "achieved": gbs, "frac": gbs / peak,
+           "frac_nominal": gbs / NOMINAL_HBM_GBS,
+           "per_call_events": {"avg_launch_ms": ev_ms, "achieved": gbs_ev, "frac": gbs_ev / peak},
+           "steps": steps, "unit": "GB/s"}
+    del Ks, Vs, Qs
+    torch.cuda.empty_cache()
+    return out
+
+
+def parity_exemptions(w, dev, B=16, seeds=4):
+    """rapid_accept on B sequences of the bench's acceptance inputs against the
+    oracle on the same inputs, for a few Philox keys: decisions and tokens must
+    agree except in the stated near-boundary bands, whose cases are counted
+    (oracle.parity.accept_exemptions)."""
+    import torch
+
+    import oracle
+    from oracle.parity import accept_exemptions
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    inp = wl.accept_inputs(w, B=B)
+    zn, qn, tn = inp.z.numpy(), inp.q.numpy(), inp.tokens.numpy()
+    pn = None if inp.parent is None else inp.parent.numpy()
+    z, q, tok = inp.z.to(dev), inp.q.to(dev), inp.tokens.to(dev)
+    par = None if inp.parent is None else inp.parent.to(dev)
+    tot = {}
+    for k in range(seeds):
+        seed = 0x5EED3000 + k
+        res = rapid.accept(z, q, tok, par, T=w.T, eta=w.eta, seed=seed)
+        torch.cuda.synchronize()
+        g = {key: v.cpu().numpy() for key, v in res.items()}
+        r = oracle.accept(zn, qn, tn, pn, T=w.T, eta=w.eta, seed=seed)
+        for key, v in accept_exemptions(zn, qn, tn, pn, w.T, w.eta, True, g, r).items():
+            tot[key] = tot.get(key, 0) + v
+    tot["batch"] = f"{B} x {w.n_q} x {w.V}, {seeds} Philox keys, T = {w.T}, eta = {w.eta}"
+    return tot
 
 
 def kv_commit_timing(w, Ks, Vs, prefix_len, dev, stream, reps=20):
@@ -809,6 +1071,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the 70B, tree, decode and d=64 workloads after the headline one")
     ap.add_argument("--workload", default=None,
                     help="named workload (default: the 32-layer 120K Llama-3.1-8B step)")
     ap.add_argument("--profile-lm-head", action="store_true",
