@@ -1039,6 +1039,33 @@ def profile_lm_head(rows=11, hidden=4096, V=128256):
         sys.exit(1)
 
 
+def profile_lm_head_accept(rows=11, hidden=4096, V=128256):
+    """Three rapid_lm_head_accept calls of one 11-row chain step (the single
+    fused kernel) against a 128256 x 4096 bf16 head, no timing."""
+    import torch
+
+    from long_context_speculative_gb300 import rapid
+    from long_context_speculative_gb300 import workloads as wl
+
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(4096)
+    H = torch.randn((rows, hidden), generator=g, device=dev).to(torch.bfloat16)
+    W = torch.empty((V, hidden), dtype=torch.bfloat16, device=dev)
+    for i in range(0, V, 16384):
+        n = min(16384, V - i)
+        W[i:i + n] = (torch.randn((n, hidden), generator=g, device=dev) * (3.0 / 64)).to(torch.bfloat16)
+    inp = wl.accept_inputs(wl.LLAMA8B_120K)
+    q, tok = inp.q.to(dev), inp.tokens.to(dev)
+    for i in range(3):
+        rapid.lm_head_accept(H, W, q, tok, None, T=1.0, eta=1.0, seed=i)
+    torch.cuda.synchronize()
+    err = rapid.rapid_device_error()
+    print(json.dumps({"profile_lm_head_accept": rows, "hidden": hidden, "vocab": V,
+                      "device_error": err}))
+    if err:
+        sys.exit(1)
+
+
 def profile_retrieval(B, N=240, D=1024):
     """Three scores + select calls on B requests of N chunks x D bf16, no timing."""
     import torch
@@ -1078,6 +1105,9 @@ def main():
     ap.add_argument("--profile-lm-head", action="store_true",
                     help="run rapid_lm_head three times on 11 x 4096 rows against a "
                          "128256 x 4096 head (for ncu) and exit")
+    ap.add_argument("--profile-lm-head-accept", action="store_true",
+                    help="run rapid_lm_head_accept three times on one 11-row step against a "
+                         "128256 x 4096 head (for ncu) and exit")
     ap.add_argument("--profile-retrieval", type=int, default=0, metavar="B",
                     help="run retrieval scores + select on B requests of 240 chunks x 1024 "
                          "(for ncu) and exit")
@@ -1093,6 +1123,9 @@ def main():
     WORKLOAD = w.name
     if args.profile_lm_head:
         profile_lm_head()
+        return
+    if args.profile_lm_head_accept:
+        profile_lm_head_accept()
         return
     if args.profile_retrieval > 0:
         profile_retrieval(args.profile_retrieval)

@@ -535,11 +535,29 @@ size_t rapid_lm_head_accept_workspace_size(int B, int n_q, int V);
 /*
  * rapid_accept on logits that rapid_lm_head computes from the verify rows'
  * hidden states [B * n_q, hidden_dim] (row b * n_q + i is node i of sequence
- * b): the two launches run back to back on `stream`, and z lives in the
- * workspace (for one verify step, 11 x 128256 fp32 = 5.6 MB, which stays in
- * L2 between them), so the caller never holds the logits.  Every other
- * argument, output and error is rapid_accept's; B * n_q is at most
- * RAPID_LM_HEAD_MAX_ROWS and V at most RAPID_MAX_VOCAB.
+ * b); the caller never holds the logits.
+ *
+ * Up to 16 rows (one verify step of an 11-node chain or a 16-node tree), V a
+ * multiple of 4 and q_draft 16-byte aligned: ONE cooperative kernel, one CTA
+ * per SM, computes the product and then the acceptance step itself.  Each CTA
+ * keeps its run of the vocabulary of z in shared memory (z is never written
+ * to memory) with the same run of q beside it; the vocabulary-wide softmax
+ * statistics, the ratio tests, the path choice and the residual draw follow,
+ * with one grid-wide barrier after each of the three vocabulary-wide
+ * reductions.  The call first zeroes a 4-byte barrier counter at the front of
+ * the workspace (a memset on `stream`); calls on one workspace must not
+ * overlap.  The arithmetic is rapid_accept's up to the order of fp32 sums, so
+ * probabilities agree with rapid_accept's to about 1e-6 relative and
+ * decisions agree except at the near-boundary cases of the ratio test, the
+ * tail threshold and the inverse CDF.
+ *
+ * Otherwise (more rows, or a device without cooperative launches) two
+ * launches run back to back on `stream`: rapid_lm_head into the workspace
+ * (11 x 128256 fp32 = 5.6 MB for one step, which stays in L2), then
+ * rapid_accept on it.
+ *
+ * Every other argument, output and error is rapid_accept's; B * n_q is at
+ * most RAPID_LM_HEAD_MAX_ROWS and V at most RAPID_MAX_VOCAB.
  */
 rapid_status rapid_lm_head_accept(const void* hidden, const void* W_lm, int hidden_dim,
                                   const float* q_draft, const int32_t* draft_tokens,

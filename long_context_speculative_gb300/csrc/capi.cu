@@ -348,11 +348,30 @@ static rapid_status lm_head_accept_impl(const void* hidden, const void* W_lm, in
     if (n_nodes && (reinterpret_cast<uintptr_t>(n_nodes) & 3u)) return RAPID_EINVAL;
     if (workspace_bytes < rapid_lm_head_accept_workspace_size(B, n_q, V)) return RAPID_ENOMEM;
     if (!lm_head_supported()) return RAPID_EUNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Up to 16 rows: one cooperative kernel does the product and the
+    // acceptance step, z stays in shared memory (its scratch is a prefix of
+    // the workspace that the two-launch form below uses for z).
+    {
+        LmAcceptParams fa{};
+        fa.q = q_draft; fa.tokens = draft_tokens; fa.parent = parent; fa.n_nodes = n_nodes;
+        fa.seed_dev = reinterpret_cast<const unsigned long long*>(philox_seed_dev);
+        fa.n_accepted = n_accepted; fa.next_token = next_token; fa.path = path; fa.diag = diag;
+        fa.B = B; fa.n_q = n_q;
+        fa.clamp = (flags & RAPID_ACCEPT_TAIL_CLAMP) ? 1 : 0;
+        fa.invT = 1.0f / T;
+        fa.eta = eta;
+        fa.seed_lo = (uint32_t)(philox_seed & 0xffffffffu);
+        fa.seed_hi = (uint32_t)(philox_seed >> 32);
+        const cudaError_t e = launch_lm_head_accept(hidden, W_lm, hidden_dim, V, fa, workspace,
+                                                    workspace_bytes, device_error_word(), st);
+        if (e == cudaSuccess) return RAPID_OK;
+        if (e != cudaErrorNotSupported) return RAPID_ECUDA;
+    }
     // z lives at the front of the workspace (B n_q V floats, L2-resident at
     // the sizes of one verify step); the acceptance scratch follows it.
     float* z = static_cast<float*>(workspace);
     void* acc_ws = static_cast<char*>(workspace) + align_up((size_t)B * n_q * V * sizeof(float));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (launch_lm_head(hidden, W_lm, B * n_q, hidden_dim, V, z, device_error_word(), st) !=
         cudaSuccess)
         return RAPID_ECUDA;

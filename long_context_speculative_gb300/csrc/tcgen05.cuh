@@ -49,6 +49,24 @@ RAPID_DEVICE void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, ui
         : "memory");
 }
 
+// L2 policy for data read once: its lines are the first to be evicted, so a
+// stream of it does not push out what later work reuses (code, partials).
+RAPID_DEVICE uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy (l2_evict_first_policy()).
+RAPID_DEVICE void tma_load_2d_hint(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
+                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // 32 consecutive TMEM columns of this warp's 32 lanes -> 32 registers per thread.
 RAPID_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

@@ -108,9 +108,10 @@ def test_lm_head_logits(rows, V):
     _check(("z", z))
 
 
-def test_lm_head_accept_workspace_and_outputs():
+@pytest.mark.parametrize("B", [1, 2])   # 11 rows: the single fused kernel; 22: two launches
+def test_lm_head_accept_workspace_and_outputs(B):
     w = wl.LLAMA8B_LAYER_32K
-    inp = wl.accept_inputs(w, B=2)
+    inp = wl.accept_inputs(w, B=B)
     q, tok = inp.q.to(DEV), inp.tokens.to(DEV)
     B, n_q, V = q.shape
     g = torch.Generator(device=DEV).manual_seed(8)

@@ -107,27 +107,89 @@ def _draft_from_logits(z, parent, T, seed):
     return q, tokens
 
 
-def _fused_case(B, n_q, hidden, V, parent, T, eta, seed):
+def _fused_case(B, n_q, hidden, V, parent, T, eta, seed, clamp=True, n_nodes=None,
+                device_key=False):
     H, W = _weights(B * n_q, hidden, V, seed=seed)
     Hf, Wf = H.float().numpy(), W.float().numpy()
     z64 = oracle.lm_head_logits(Hf, Wf)
     z_ref = z64.reshape(B, n_q, V).astype(np.float32)
     q, tokens = _draft_from_logits(z_ref.astype(np.float64), parent, T, seed + 1)
-    # the logits the fused call computes (the same kernel), within their bound;
-    # their largest deviation sets how far the probabilities may move
+    # the logits the fused call computes (the same product), within their
+    # bound; their largest deviation sets how far the probabilities may move
     dz = _check_logits(_gpu_logits(H, W), Hf, Wf)
     band = 1e-5 + 2.0 * dz / T
-    ref = oracle.accept(z_ref, q, tokens, parent, T=T, eta=eta, seed=seed + 2, clamp=True)
+    ref = oracle.accept(z_ref, q, tokens, parent, T=T, eta=eta, seed=seed + 2, clamp=clamp,
+                        n_nodes=n_nodes)
     par_d = None if parent is None else torch.from_numpy(parent.astype(np.int32)).to(DEV)
-    out = rapid.lm_head_accept(H.to(DEV), W.to(DEV), torch.from_numpy(q).to(DEV),
-                               torch.from_numpy(tokens).to(DEV), par_d, T=T, eta=eta,
-                               seed=seed + 2)
+    dev = lambda a: torch.from_numpy(a).to(DEV)
+    if n_nodes is None and not device_key:
+        out = rapid.lm_head_accept(H.to(DEV), W.to(DEV), dev(q), dev(tokens), par_d, T=T,
+                                   eta=eta, seed=seed + 2, tail_clamp=clamp)
+    else:
+        out = dict(n_accepted=torch.empty(B, dtype=torch.int32, device=DEV),
+                   next_token=torch.empty(B, dtype=torch.int32, device=DEV),
+                   path=torch.empty((B, n_q), dtype=torch.int32, device=DEV),
+                   diag=torch.empty((B, n_q, 5), dtype=torch.float32, device=DEV))
+        ws = torch.empty(rapid.rapid_lm_head_accept_workspace_size(B, n_q, V),
+                         dtype=torch.uint8, device=DEV)
+        key = (torch.tensor([seed + 2], dtype=torch.int64, device=DEV) if device_key
+               else seed + 2)
+        rapid.rapid_lm_head_accept_ex(H.to(DEV), W.to(DEV), dev(q), dev(tokens), par_d,
+                                      None if n_nodes is None else dev(n_nodes.astype(np.int32)),
+                                      T, eta, key, rapid.RAPID_ACCEPT_TAIL_CLAMP if clamp else 0,
+                                      out["n_accepted"], out["next_token"], out["path"],
+                                      out["diag"], ws)
     torch.cuda.synchronize()
     gpu = {k: (v.cpu().numpy() if v is not None else None) for k, v in out.items()}
-    stats = check_accept(z_ref, q, tokens, parent, T, eta, seed + 2, True, gpu, ref,
-                         prob_rtol=band, exempt=band)
+    stats = check_accept(z_ref, q, tokens, parent, T, eta, seed + 2, clamp, gpu, ref,
+                         prob_rtol=band, exempt=band, n_nodes=n_nodes)
     assert rapid.rapid_device_error(True) == 0
     return stats
+
+
+def _random_tree(B, n_q, seed):
+    rng = np.random.default_rng(seed)
+    parent = np.zeros((B, n_q), np.int32)
+    parent[:, 0] = -1
+    for b in range(B):
+        for i in range(1, n_q):
+            parent[b, i] = rng.integers(0, i)
+    return parent
+
+
+# Up to 16 rows the fused call is one cooperative kernel: the product, then the
+# acceptance step with z kept in shared memory.  Shapes: the Llama-3.1-8B
+# vocabulary (one 11-row chain step), the Qwen2.5-7B vocabulary with a 16-node
+# tree, a vocabulary smaller than one CTA per SM, eta above the bound of 32,
+# the tail rule off, a single query row (bonus draw only).
+@pytest.mark.parametrize("B,n_q,hidden,V,tree,T,eta,clamp", [
+    (1, 11, 1024, 128256, False, 1.0, 1.0, True),
+    (1, 16, 512, 152064, True, 1.0, 1.0, True),
+    (2, 8, 512, 50000, False, 0.6, 5.0, True),
+    (1, 11, 512, 32000, False, 1.0, 40.0, True),
+    (4, 4, 256, 1000, True, 1.0, 1.0, True),
+    (2, 6, 256, 20000, False, 1.0, 10.0, False),
+    (1, 1, 1024, 128256, False, 1.0, 1.0, True),
+    (3, 5, 256, 4100, True, 0.8, 0.0, True),
+])
+def test_fused_single_kernel_shapes(B, n_q, hidden, V, tree, T, eta, clamp):
+    parent = _random_tree(B, n_q, seed=V + n_q) if tree else None
+    tot = {}
+    for k in range(3):
+        st = _fused_case(B, n_q, hidden, V, parent, T, eta, seed=100 * k + B + V % 97,
+                         clamp=clamp)
+        for key, v in st.items():
+            tot[key] = tot.get(key, 0) + v
+    assert tot["compared"] >= 2 * B
+
+
+def test_fused_single_kernel_ragged_and_device_key():
+    B, n_q, V = 2, 8, 30000
+    parent = _random_tree(B, n_q, seed=5)
+    n_nodes = np.array([8, 3], np.int32)
+    st = _fused_case(B, n_q, 512, V, parent, 1.0, 1.0, seed=55, n_nodes=n_nodes,
+                     device_key=True)
+    assert st["compared"] + st["ratio_exempt"] + st["clamp_exempt"] >= 1
 
 
 @pytest.mark.parametrize("T,eta", [(1.0, 1.0), (0.6, 0.0), (1.0, 5.0)])
