@@ -254,6 +254,13 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     } else if (warp == kProducerWarp) {
         // ------------------------------ TMA producer --------------------------
         if (lane == 0) {
+            // A K/V tile read by one CTA only is dead after its copy: with a
+            // single row block its L2 lines go first when L2 needs room, so
+            // the stream does not push out the partials and code that the
+            // merge and the next launches reuse.  Wider groups keep the
+            // default policy: the second row block re-reads each tile from L2.
+            const uint64_t kv_policy = l2_evict_first_policy();
+            const bool once = n_rb == 1;
             // Tile i's rows in the cache (the speculative tile starts at P).
             auto tile_y = [&](int i) -> int {
                 const int64_t row0 = (i < n_hist) ? (int64_t)(t_begin + i) * kKeys : P;
@@ -276,8 +283,15 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 mbar_arrive_expect_tx(&bars->kv_full[st], kStageBytes);
 #pragma unroll
                 for (int c = 0; c < L::kDBlocks; ++c) {   // 64-column blocks of K, then V
-                    tma_load_2d(kt + c * kBlockBytes, &tmK, 64 * c, y, &bars->kv_full[st]);
-                    tma_load_2d(vt + c * kBlockBytes, &tmV, 64 * c, y, &bars->kv_full[st]);
+                    if (once) {
+                        tma_load_2d_hint(kt + c * kBlockBytes, &tmK, 64 * c, y, &bars->kv_full[st],
+                                         kv_policy);
+                        tma_load_2d_hint(vt + c * kBlockBytes, &tmV, 64 * c, y, &bars->kv_full[st],
+                                         kv_policy);
+                    } else {
+                        tma_load_2d(kt + c * kBlockBytes, &tmK, 64 * c, y, &bars->kv_full[st]);
+                        tma_load_2d(vt + c * kBlockBytes, &tmV, 64 * c, y, &bars->kv_full[st]);
+                    }
                 }
             }
             if (*((volatile int*)&bars->abort)) {
