@@ -371,9 +371,13 @@ accept_rows_kernel(const AcceptParams p) {
         }
         mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 8));
         if (n > 0) {
+            // rows are read once here (the selection re-reads at most one row
+            // of a sequence, which it prefetches itself): evict-first, so the
+            // stream does not push the selection's code and inputs out of L2
             const int64_t off = row_of(i) * p.V + lo;
-            bulk_g2s(zb, p.z + off, (uint32_t)(n * 4), &sh.full[g]);
-            bulk_g2s(qb, p.q + off, (uint32_t)(n * 4), &sh.full[g]);
+            const uint64_t pol = l2_policy_evict_first();
+            bulk_g2s_hint(zb, p.z + off, (uint32_t)(n * 4), &sh.full[g], pol);
+            bulk_g2s_hint(qb, p.q + off, (uint32_t)(n * 4), &sh.full[g], pol);
         }
     };
     // L2 prefetch of a later row of this group, so that its bulk copy, issued

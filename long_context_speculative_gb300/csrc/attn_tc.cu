@@ -259,7 +259,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             // the stream does not push out the partials and code that the
             // merge and the next launches reuse.  Wider groups keep the
             // default policy: the second row block re-reads each tile from L2.
-            const uint64_t kv_policy = l2_evict_first_policy();
+            const uint64_t kv_policy = l2_policy_evict_first();
             const bool once = n_rb == 1;
             // Tile i's rows in the cache (the speculative tile starts at P).
             auto tile_y = [&](int i) -> int {

@@ -226,6 +226,24 @@ RAPID_DEVICE void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t*
         : "memory");
 }
 
+// bulk_g2s with an L2 cache policy (for example evict-first for data that is
+// read once, so that its stream does not push other data and code out of L2).
+RAPID_DEVICE void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read once: its lines are the first to be evicted.
+RAPID_DEVICE uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk prefetch of global memory into L2 (no completion to wait for).
 // src 16-byte aligned; bytes a multiple of 16.
 RAPID_DEVICE void bulk_prefetch_l2(const void* src, uint32_t bytes) {

@@ -177,7 +177,7 @@ lm_head_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ 
                                  (uint32_t)(v_real * 4), &bars->q_full);
             }
             // the head is read once: its lines go first when L2 needs room
-            const uint64_t w_policy = l2_evict_first_policy();
+            const uint64_t w_policy = l2_policy_evict_first();
             int it = 0, issued = 0;
             bool ok = true;
             for (int j = 0; j < n_tiles && ok; ++j) {

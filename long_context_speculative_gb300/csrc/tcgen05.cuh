@@ -49,15 +49,8 @@ RAPID_DEVICE void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, ui
         : "memory");
 }
 
-// L2 policy for data read once: its lines are the first to be evicted, so a
-// stream of it does not push out what later work reuses (code, partials).
-RAPID_DEVICE uint64_t l2_evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-// tma_load_2d with an L2 cache policy (l2_evict_first_policy()).
+// tma_load_2d with an L2 cache policy (l2_policy_evict_first() for data read
+// once, so that its stream does not push out what later work reuses).
 RAPID_DEVICE void tma_load_2d_hint(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
                                    uint64_t policy) {
     asm volatile(
