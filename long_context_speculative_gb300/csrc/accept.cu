@@ -364,11 +364,16 @@ accept_rows_kernel(const AcceptParams p) {
         const int b = (int)(row / p.n_q);
         return (int)(row - (int64_t)b * p.n_q) >= node_count(p, b);
     };
-    auto load_row = [&](int i) {      // one thread, bulk path
-        if (padding(i)) {             // completes the buffer's phase with nothing to land
-            mbar_arrive(&sh.full[g]);
-            return;
-        }
+    // The group's first row at or after i that is not padding (i, i + 2, ...),
+    // or nrows.  Padding rows take no buffer phase: the k-th real row of the
+    // group is the k-th phase of its buffer barrier, so a warp can never wait
+    // on a phase two ahead of the barrier (which would pass at once, on the
+    // phase before).
+    auto next_real = [&](int i) -> int {
+        while (i < nrows && padding(i)) i += 2;
+        return i;
+    };
+    auto load_row = [&](int i) {      // one thread, bulk path, a row that is not padding
         mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 8));
         if (n > 0) {
             // rows are read once here (the selection re-reads at most one row
@@ -382,14 +387,17 @@ accept_rows_kernel(const AcceptParams p) {
     };
     // L2 prefetch of a later row of this group, so that its bulk copy, issued
     // only once the buffer is free, is served from L2
-    auto prefetch_row = [&](int i) {   // one thread, bulk path
-        if (i < nrows && n > 0 && !padding(i)) {
+    auto prefetch_row = [&](int i) {   // one thread, bulk path, a real row or nrows
+        if (i < nrows && n > 0) {
             const int64_t off = row_of(i) * p.V + lo;
             bulk_prefetch_l2(p.z + off, (uint32_t)(n * 4));
             bulk_prefetch_l2(p.q + off, (uint32_t)(n * 4));
         }
     };
-    if (p.bulk && tg == 0 && g < nrows) load_row(g);
+    if (p.bulk && tg == 0) {
+        const int j0 = next_real(g);
+        if (j0 < nrows) load_row(j0);
+    }
 
     // The group's last two warps run the ratio tests: thread tg handles child
     // c = tg - (kGT - kAcceptMaxNq).  Its token and parent are loaded a row ahead.
@@ -411,28 +419,17 @@ accept_rows_kernel(const AcceptParams p) {
     // independently; the last warp of a phase combines the group's partials
     // and sends them to the cluster, and every warp waits for the cluster's
     // partials itself.  The other group computes while this one waits.
-    // Row i of the cluster's list is the group's (i >> 1)-th row: the phase of
-    // full[g].  kx counts the rows the group has exchanged (padding rows are
-    // not): the phase of mb1[g] and mb2[g].
+    // kx counts the group's rows that are not padding: the phase of full[g],
+    // mb1[g] and mb2[g] for the row at hand.
     int kx = 0;
 #pragma unroll 1
     for (int i = g; i < nrows; i += 2) {
         const int64_t row = row_of(i);
         const int b = (int)(row / p.n_q);
         const int j = (int)(row - (int64_t)b * p.n_q);
-        if (padding(i)) {
-            // The buffer's phase for this row completed without a copy.  The
-            // group's warps last read the buffer in pass 2 of an earlier row,
-            // and thread 0 got here only after that row's reduction 2, which
-            // needs every warp's pass 2: the next row may take the buffer now.
+        if (padding(i)) {   // no copy, no exchange, no buffer phase
             prefetch_node(i + 2);
-            if (tg == 0) {
-                if (i == 0) mbar_arrive(&sh.stagger);
-                if (p.bulk && i + 2 < nrows) {
-                    fence_proxy_async_smem();
-                    load_row(i + 2);
-                }
-            }
+            if (tg == 0 && i == 0) mbar_arrive(&sh.stagger);
             continue;
         }
         if (tg == 0) {
@@ -440,7 +437,7 @@ accept_rows_kernel(const AcceptParams p) {
             // before any warp of the group could finish the previous row)
             mbar_arrive_expect_tx(&sh.mb1[g], (uint32_t)(C * 8));
             mbar_arrive_expect_tx(&sh.mb2[g], (uint32_t)(C * 12));
-            if (p.bulk) prefetch_row(i + 2);
+            if (p.bulk) prefetch_row(next_real(i + 2));
         }
         const int my_tok = pf_tok, my_par = pf_par;
         prefetch_node(i + 2);
@@ -449,7 +446,7 @@ accept_rows_kernel(const AcceptParams p) {
         if (i == 1)
             wait_or_abort(&sh.stagger, 0u, &sh.abort, p.err, 0x06000000u);
         if (p.bulk) {
-            wait_or_abort(&sh.full[g], (uint32_t)((i >> 1) & 1), &sh.abort, p.err,
+            wait_or_abort(&sh.full[g], (uint32_t)(kx & 1), &sh.abort, p.err,
                           0x01000000u | (unsigned)(i & 0xffff));
         } else {
             const int64_t off = row * p.V + lo;
@@ -516,11 +513,14 @@ accept_rows_kernel(const AcceptParams p) {
                     st_async_v2(mapa_u32(smem_u32(&sh.recv2[g][rank]), (uint32_t)lane), c2.m, c2.s, rbar);
                     st_async_f32(mapa_u32(smem_u32(&sh.recv2a[g][rank]), (uint32_t)lane), ac, rbar);
                 }
-                if (lane == 0 && p.bulk && i + 2 < nrows) {
+                if (lane == 0 && p.bulk) {
                     // every warp of the group is done with the buffer: it takes
                     // the group's next row while reduction 2 travels
-                    fence_proxy_async_smem();
-                    load_row(i + 2);
+                    const int jn = next_real(i + 2);
+                    if (jn < nrows) {
+                        fence_proxy_async_smem();
+                        load_row(jn);
+                    }
                 }
             }
         }
@@ -571,7 +571,8 @@ accept_rows_kernel(const AcceptParams p) {
         if (p.bulk && sh.abort) {
             // a wait gave up: let the groups' last copies land before the CTA exits
             for (int gg = 0; gg < kGroups; ++gg) {
-                const int nmine = nrows > gg ? (nrows - gg + 1) / 2 : 0;
+                int nmine = 0;   // the group's real rows: one buffer phase each
+                for (int i = gg; i < nrows; i += 2) nmine += padding(i) ? 0 : 1;
                 if (nmine > 0) mbar_wait(&sh.full[gg], (uint32_t)((nmine - 1) & 1), nullptr);
             }
         }

@@ -169,6 +169,10 @@ _RAGGED = {
     # more rows than clusters, seeded lengths
     "chain_seeded_20": (wl.LLAMA8B_LAYER_32K,
                         np.random.default_rng(8).integers(1, 12, size=20).tolist()),
+    # long runs of padding rows between a cluster's real rows: a warp group may
+    # skip several padding rows while its first thread is still issuing the
+    # previous row's copy (padding rows take no buffer phase)
+    "sparse_40": (wl.LLAMA8B_LAYER_32K, ([1] * 9 + [11]) * 4),
 }
 
 
