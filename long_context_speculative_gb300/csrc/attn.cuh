@@ -110,11 +110,19 @@ __device__ __forceinline__ SplitOf split_of(const AttnParams& p, int pairs, int 
     return SplitOf{-1, 0, 0, 0};
 }
 
+// Row blocks of the tensor-core kernel for a group of R rows: one CTA per
+// (split, block) covers up to 128 rows, or 256 (two row blocks that share
+// every K/V tile) when the group has more than 128.
+__host__ __device__ __forceinline__ int tc_row_blocks(int R) {
+    const int per_cta = R <= 128 ? 128 : 256;
+    return (R + per_cta - 1) / per_cta;
+}
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_attn_prefix_simt(const AttnParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_attn_merge(const AttnParams& p, int dtype, cudaStream_t s);
 // tcgen05 + TMA prefix kernel (bf16 caches, d = 64 or 128, up to 512 group
-// rows R = G * n_q, run as 128-row blocks).  attn_prefix_tc_supported() says
+// rows R = G * n_q, run as blocks of 128 rows, or of 256 above 128 rows).  attn_prefix_tc_supported() says
 // whether a shape is one it handles.
 cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t s);
 bool attn_prefix_tc_supported(const AttnParams& p, int dtype);

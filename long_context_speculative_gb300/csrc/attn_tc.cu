@@ -1,6 +1,6 @@
-// Tensor-core history kernel of verify attention (bf16, head_dim 128, up to
-// 128 query rows per KV-head group), written for sm_103a: TMA-staged K/V
-// tiles, tcgen05 MMAs with accumulators in tensor memory, warp-specialised.
+// Tensor-core history kernel of verify attention (bf16, head_dim 64 or 128,
+// up to 512 query rows per KV-head group), written for sm_103a: TMA-staged
+// K/V tiles, tcgen05 MMAs with accumulators in tensor memory, warp-specialised.
 //
 // Hybrid tree attention ("LongSpec: Long-Context Lossless Speculative
 // Decoding with Efficient Drafting and Verification", section 2.3) needs no
@@ -11,8 +11,10 @@
 //
 // CTA = (split s, sequence b * Hkv + KV head g); 352 threads:
 //   warps 0-7  softmax, in two consumer groups (warps 0-3 take the even
-//              tiles of the split, warps 4-7 the odd ones); warp w owns TMEM
-//              lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.  A
+//              tiles of the split, warps 4-7 the odd ones; in a 256-row CTA
+//              they are its two 128-row blocks and both take every tile);
+//              warp w owns TMEM lane quadrant w % 4, i.e. rows 32 (w % 4) ..
+//              + 31 of its group's M = 128 operand.  A
 //              group turns its S tile into P (bf16, its own shared buffer),
 //              keeps its running max / sum and rescales its O in TMEM when the
 //              max grows by more than 2^8.  At the end the two groups combine
@@ -56,22 +58,29 @@ constexpr uint32_t kTmemO = 256;
 constexpr int kBarBytes = 512;
 
 // Shared-memory plan for ROWS query rows kept on chip (64 when the group has
-// at most 64 rows, else 128) and head dimension D (64 or 128).  The MMAs
-// always run with M = 128: with ROWS = 64 the operand rows 64..127 of Q and P
-// read the neighbouring shared data and only produce output rows that are
-// never used, which frees room for more K/V stages.  The ring takes what
-// shared memory is left: 6 / 5 stages of 32 KB at D = 128, 12 / 11 stages of
-// 16 KB at D = 64 (the same bytes in flight).
+// at most 64 rows, 128 when it has at most 128, else 256) and head dimension D
+// (64 or 128).  The MMAs always run with M = 128: with ROWS = 64 the operand
+// rows 64..127 of Q and P read the neighbouring shared data and only produce
+// output rows that are never used, which frees room for more K/V stages.
+// With ROWS = 256 the two consumer groups are the two 128-row blocks of the
+// CTA, and each takes every tile: a K/V tile copied into the SM then serves
+// 256 query rows instead of 128, which halves the bytes an SM has to take in
+// per row of work (the copies in flight, not the HBM bandwidth, bound a CTA
+// that runs 128 rows per tile).  The ring takes what shared memory is left:
+// 6 / 5 / 4 stages of 32 KB at D = 128, 12 / 11 / 10 stages of 16 KB at D = 64.
 template <int ROWS, int D>
 struct Plan {
     static constexpr int kD = D;
+    static constexpr bool kRowGroups = ROWS > 128;       // groups = row blocks, not even / odd tiles
+    static constexpr int kCtaRows = kRowGroups ? 256 : 128;   // group rows one CTA covers
+    static constexpr int kGroupRows = kRowGroups ? 128 : ROWS;
     static constexpr int kDBlocks = D / 64;              // 64-column blocks of Q, K and V
     static constexpr int kTileBytes = kKeys * D * 2;     // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;   // K + V
-    static constexpr int kActiveQuadrants = ROWS / 32;   // softmax warps per group
+    static constexpr int kActiveQuadrants = kGroupRows / 32;   // softmax warps per group
     static constexpr int kGroupThreads = 32 * kActiveQuadrants;
     static constexpr int kQBlock = ROWS * 128;           // one 64-column block of Q
-    static constexpr int kPBytes = ROWS * 128;           // one P buffer (64 keys)
+    static constexpr int kPBytes = kGroupRows * 128;     // one P buffer (64 keys)
     static constexpr int kOffQ = 0;
     static constexpr int kOffP = kOffQ + kDBlocks * kQBlock;
     static constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
@@ -83,6 +92,7 @@ struct Plan {
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     static_assert(D == 64 || D == 128, "head dimension 64 or 128");
+    static_assert(ROWS == 64 || ROWS == 128 || ROWS == 256, "64, 128 or 256 rows");
     static_assert(kStages >= 4, "too few stages");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -155,11 +165,11 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     // stream the same K/V tiles together and the second read of each tile is
     // served from L2.  Which (sequence, split) a slot holds is decided on the
     // device from the prefix lengths (split_of), after griddep_wait().
-    const int n_rb = (p.R + 127) / 128;
+    const int n_rb = tc_row_blocks(p.R);
     const int slot_idx = blockIdx.x / n_rb;
     const int rb = blockIdx.x - slot_idx * n_rb;
-    const int r0 = rb * 128;                       // first group row of this CTA
-    const int Rb = min(128, p.R - r0);             // rows of this CTA
+    const int r0 = rb * L::kCtaRows;               // first group row of this CTA
+    const int Rb = min(L::kCtaRows, p.R - r0);     // rows of this CTA
     const int g = blockIdx.y;
     // Input-free set-up first: it may overlap the previous kernel in the stream.
     if (tid == 0) {
@@ -315,9 +325,83 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             const uint64_t kd0 = sdesc(smem_base + kOffKV, 16, 1024);
             const uint64_t pd0 = sdesc(smem_base + kOffP, 16, 1024);
             const uint64_t vd0 = sdesc(smem_base + kOffKV + kTileBytes, kBlockBytes, 1024);
-            int next_s = 0, next_pv = 0;
             bool ok = true;
             uint64_t t_last = global_timer_ns();
+            if constexpr (L::kRowGroups) {
+                // The two row blocks move through the tiles together, and
+                // their products are issued in pairs, one K step of each
+                // block in turn: successive MMAs into the same accumulator
+                // wait for each other in the tensor pipe, MMAs into the
+                // other block's accumulator do not.  S_j of both blocks
+                // goes to buffer j & 1, free once the PV pair of tile j - 2
+                // was issued; tile j's ring slot is released after its PV pair.
+                int ns = 0, npv = 0;
+                while (npv < n) {
+                    bool progressed = false;
+                    if (npv < ns && mbar_try_wait(&bars->p_full[0], npv & 1) &&
+                        mbar_try_wait(&bars->p_full[1], npv & 1)) {
+                        tc_fence_after();
+                        const int i = npv;
+                        const int st = i % kStages;
+                        const uint64_t vd = vd0 + (uint64_t)(st * (kStageBytes >> 4));
+#pragma unroll
+                        for (int k = 0; k < kKeys / 16; ++k) {
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+                                mma_bf16(tmem + kTmemO + (uint32_t)(u * kD),
+                                         pd0 + (uint64_t)(u * (kPBytes >> 4) + k * 2),
+                                         vd + (uint64_t)(k * (2048 >> 4)), L::kIdescPV,
+                                         (i > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars->p_free[0]);
+                        mma_commit(&bars->p_free[1]);
+                        mma_commit(&bars->kv_empty[st]);
+                        ++npv;
+                        progressed = true;
+                    }
+                    if (ns < n && ns <= npv + 1 &&
+                        mbar_try_wait(&bars->kv_full[ns % kStages], (ns / kStages) & 1)) {
+                        tc_fence_after();
+                        const int j = ns;
+                        const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
+#pragma unroll
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint64_t qoff = (uint64_t)(((k >> 2) * L::kQBlock + (k & 3) * 32) >> 4);
+                            const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)   // block u: Q rows 128 u .. + 127
+                                mma_bf16(tmem + kTmemS + (uint32_t)((2 * u + (j & 1)) * kKeys),
+                                         qd0 + qoff + (uint64_t)(u * ((128 * 128) >> 4)), kd + koff,
+                                         kIdescS, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full[j & 1]);
+                        mma_commit(&bars->s_full[2 + (j & 1)]);
+                        ++ns;
+                        progressed = true;
+                    }
+                    if (progressed) {
+                        t_last = global_timer_ns();
+                    } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
+                        if (npv < ns) {
+                            // a PV pair is next: wait for the block that is not there yet
+                            if (mbar_try_wait(&bars->p_full[0], npv & 1))
+                                (void)mbar_try_wait_sleep(&bars->p_full[1], npv & 1, 500u);
+                            else
+                                (void)mbar_try_wait_sleep(&bars->p_full[0], npv & 1, 500u);
+                        } else if (ns < n) {
+                            (void)mbar_try_wait_sleep(&bars->kv_full[ns % kStages], (ns / kStages) & 1,
+                                                      500u);
+                        }
+                    } else {
+                        atomicOr(p.err, kErrWaitTimeout);
+                        atomicCAS(p.err + 1, 0u,
+                                  0x80000000u | kRoleMma | kBarPFull | (unsigned)(npv & 0xffff));
+                        ok = false;
+                        break;
+                    }
+                }
+            } else {
+            int next_s = 0, next_pv = 0;
             while (next_pv < n) {
                 bool progressed = false;
                 if (next_s < n && next_s <= next_pv + 3 &&
@@ -375,6 +459,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                     break;
                 }
             }
+            }
             if (!ok) bars->abort = 1;
             // drain: every MMA issued so far has completed once this arrives
             mma_commit(&bars->drain);
@@ -382,19 +467,21 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
     } else if (warp < kSoftmaxWarps && (warp & 3) < L::kActiveQuadrants) {
         // ------------------------------ softmax warps -------------------------
-        // Group gr = warp / 4 takes tiles gr, gr + 2, ...; warp w owns TMEM
-        // lane quadrant w % 4, i.e. query rows 32 (w % 4) .. + 31.
+        // Group gr = warp / 4 takes tiles gr, gr + 2, ... (with ROWS = 256:
+        // every tile, for row block gr); warp w owns TMEM lane quadrant w % 4,
+        // i.e. rows 32 (w % 4) .. + 31 of the group's 128-row operand.
         const int q4 = warp & 3;
         const int gr = warp >> 2;
-        const int r = q4 * 32 + lane;                         // query row = TMEM lane
+        const int r = q4 * 32 + lane;                         // operand row = TMEM lane
+        const int rr = (L::kRowGroups ? gr * 128 : 0) + r;    // query row of the CTA
         const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t o_col = kTmemO + (uint32_t)(gr * kD);
         const float c = p.scale_log2;
         const int64_t key_end = ((int64_t)t_end * kKeys < P) ? (int64_t)t_end * kKeys : P;
         // visibility of the n_q speculative keys for this row (the masked tile)
         uint64_t spec_bits = 0;
-        if (spec_here && ((n - 1) & 1) == gr && r < Rb) {
-            const int iq = (r0 + r) % p.n_q;
+        if (spec_here && (L::kRowGroups || ((n - 1) & 1) == gr) && rr < Rb) {
+            const int iq = (r0 + rr) % p.n_q;
             for (int j = 0; j < p.n_q; ++j) {
                 const bool vis =
                     p.mask ? (p.mask[((int64_t)b * p.n_q + iq) * p.n_q + j] != 0) : (j <= iq);
@@ -404,7 +491,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int k_local = 0;
-        for (int i = gr; i < n; i += 2, ++k_local) {
+        constexpr int kStep = L::kRowGroups ? 1 : 2;
+        for (int i = L::kRowGroups ? 0 : gr; i < n; i += kStep, ++k_local) {
             const int sbuf = 2 * gr + (k_local & 1);
             const uint32_t s_col = kTmemS + (uint32_t)(sbuf * kKeys);
             ok = __all_sync(0xffffffffu,
@@ -498,6 +586,37 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             ok = __all_sync(0xffffffffu,
                             mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
                                             kRoleSoftmax | kBarPFree | 0xffffu));
+        if constexpr (L::kRowGroups) {
+            // Each group owns its rows' partial: (O, m, l) as they stand.
+            if (ok) {
+                tc_fence_after();
+                const bool real_row = rr < Rb;
+                const bool has = k_local > 0 && l_run > 0.f;
+                float* dst = p.part_acc + (slot + r0 + rr) * kD;
+#pragma unroll
+                for (int qq = 0; qq < kD / 32; ++qq) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + o_col + qq * 32, o);
+                    tmem_wait_ld();
+                    if (real_row) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            float4 v;
+                            v.x = has ? __uint_as_float(o[j]) : 0.f;
+                            v.y = has ? __uint_as_float(o[j + 1]) : 0.f;
+                            v.z = has ? __uint_as_float(o[j + 2]) : 0.f;
+                            v.w = has ? __uint_as_float(o[j + 3]) : 0.f;
+                            *reinterpret_cast<float4*>(dst + qq * 32 + j) = v;
+                        }
+                    }
+                }
+                if (real_row) {
+                    p.part_ml[(slot + r0 + rr) * 2 + 0] = k_local > 0 ? m_run : -INFINITY;
+                    p.part_ml[(slot + r0 + rr) * 2 + 1] = k_local > 0 ? l_run : 0.f;
+                }
+            }
+            if (!ok) bars->abort = 1;
+        } else {
         // (m, l) of this group go into its own P buffer, which its last PV
         // product has finished reading.
         float* pub = reinterpret_cast<float*>(smem + kOffP + gr * kPBytes);
@@ -548,6 +667,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             }
         }
         if (!ok) bars->abort = 1;
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -576,7 +696,7 @@ bool make_kv_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
 
 bool attn_prefix_tc_supported(const AttnParams& p, int dtype) {
     if (dtype != 1 || (p.d != 64 && p.d != 128)) return false;
-    if (p.R < 1 || p.R > 512) return false;      // up to four 128-row blocks
+    if (p.R < 1 || p.R > 512) return false;      // up to two 256-row blocks
     if ((int64_t)p.B * p.Hkv * p.cap >= ((int64_t)1 << 31)) return false;
     return tensor_map_encoder() != nullptr;
 }
@@ -591,7 +711,7 @@ cudaError_t launch_rows(const CUtensorMap& tmK, const CUtensorMap& tmV, const At
                                          Plan<ROWS, D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.S * ((p.R + 127) / 128), p.Hkv, 1);
+    cfg.gridDim = dim3(p.S * tc_row_blocks(p.R), p.Hkv, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = Plan<ROWS, D>::kSmemBytes;
     cfg.stream = st;
@@ -610,9 +730,12 @@ cudaError_t launch_attn_prefix_tc(const AttnParams& p, cudaStream_t st) {
     const uint64_t rows = (uint64_t)p.B * p.Hkv * p.cap;
     if (!make_kv_map(&tmK, p.K, rows, p.d) || !make_kv_map(&tmV, p.V, rows, p.d))
         return cudaErrorInvalidValue;
-    if (p.d == 64)
-        return p.R <= 64 ? launch_rows<64, 64>(tmK, tmV, p, st) : launch_rows<128, 64>(tmK, tmV, p, st);
-    return p.R <= 64 ? launch_rows<64, 128>(tmK, tmV, p, st) : launch_rows<128, 128>(tmK, tmV, p, st);
+    if (p.d == 64) {
+        if (p.R <= 64) return launch_rows<64, 64>(tmK, tmV, p, st);
+        return p.R <= 128 ? launch_rows<128, 64>(tmK, tmV, p, st) : launch_rows<256, 64>(tmK, tmV, p, st);
+    }
+    if (p.R <= 64) return launch_rows<64, 128>(tmK, tmV, p, st);
+    return p.R <= 128 ? launch_rows<128, 128>(tmK, tmV, p, st) : launch_rows<256, 128>(tmK, tmV, p, st);
 }
 
 }  // namespace rapid

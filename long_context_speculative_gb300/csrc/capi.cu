@@ -76,9 +76,9 @@ AttnPlan plan_attn(int B, int Hq, int Hkv, int d, int n_q, int64_t cap, int dtyp
     int64_t chunk;
     if (pl.tc) {
         // One CTA per SM, one wave: (sequence, split) slots per KV head, times
-        // the 128-row blocks of a wide group.  The kernel decides on the
-        // device how the slots are shared out over the sequences.
-        const int64_t per_slot = (int64_t)Hkv * ((R + 127) / 128);
+        // the row blocks of a wide group.  The kernel decides on the device
+        // how the slots are shared out over the sequences.
+        const int64_t per_slot = (int64_t)Hkv * tc_row_blocks(R);
         int64_t S = sms / per_slot;
         if (S < B) S = B;
         pl.S = (int)S;

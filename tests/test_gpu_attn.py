@@ -84,10 +84,12 @@ def test_group_widths(G, n_q, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False)])
+@pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False),
+                                        (16, 20, True), (8, 64, False)])
 def test_pair_widths_ragged(G, n_q, tree, d):
-    # 129..256 group rows run as two 128-row-block CTAs that stream the same
-    # K/V tiles; ragged prefixes include an empty history and a single key
+    # 129..256 group rows run as one CTA whose two 128-row blocks take every
+    # K/V tile; 257..512 as two such CTAs (320 and 512 rows here); ragged
+    # prefixes include an empty history and a single key
     w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=d, n_q=n_q, prefix=2100, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, tree=tree,
                     tree_nodes_max_depth=6, seed=60 + G + n_q)
@@ -216,7 +218,7 @@ def test_other_full_size_shapes_sampled_rows(name, variant):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 def test_qwen_tree_shape_sampled_rows(variant):
-    # 224 group rows: two 128-row-block CTAs per split; four ragged histories
+    # 224 group rows: one CTA of two 128-row blocks per split; four ragged histories
     w = wl.QWEN7B_TREE
     a = wl.attn_inputs(w, device=DEV, layer=0, **_variant(variant, w.prefix))
     _check_sampled(a, a.mask, _sampled_rows(w, 1), f"{w.name} layer 0 {variant}")
