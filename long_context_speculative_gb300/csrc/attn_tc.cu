@@ -52,8 +52,11 @@ constexpr int kKeys = 64;                       // keys per K/V tile
 constexpr int kBlockBytes = kKeys * 128;        // one 64-column block of a K or V tile (8 KB)
 constexpr int kMaxStages = 12;
 // TMEM columns: S of group g, buffer u at 64 (2 g + u); O of group g at 256 + D g.
+// In a 256-row CTA S is single-buffered (block g at 64 g) and Q sits at 128
+// (block g at 128 + D g / 2).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemQ = 128;
 constexpr uint32_t kTmemO = 256;
 constexpr int kBarBytes = 512;
 
@@ -81,9 +84,12 @@ struct Plan {
     static constexpr int kGroupThreads = 32 * kActiveQuadrants;
     static constexpr int kQBlock = ROWS * 128;           // one 64-column block of Q
     static constexpr int kPBytes = kGroupRows * 128;     // one P buffer (64 keys)
+    // A 256-row CTA keeps Q in tensor memory (the S products then read only K
+    // from shared memory) and double-buffers each block's P in the room that frees.
+    static constexpr int kPBufs = kRowGroups ? 4 : 2;
     static constexpr int kOffQ = 0;
-    static constexpr int kOffP = kOffQ + kDBlocks * kQBlock;
-    static constexpr int kOffKV = kOffP + 2 * kPBytes;   // one P buffer per consumer group
+    static constexpr int kOffP = kOffQ + (kRowGroups ? 0 : kDBlocks * kQBlock);
+    static constexpr int kOffKV = kOffP + kPBufs * kPBytes;
     static constexpr int kFit = (232448 - 1024 - kBarBytes - kOffKV) / kStageBytes;
     static constexpr int kStages = kFit < kMaxStages ? kFit : kMaxStages;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
@@ -111,6 +117,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -127,9 +139,13 @@ enum : unsigned int {
 struct Bars {
     uint64_t kv_full[kMaxStages];
     uint64_t kv_empty[kMaxStages];
-    uint64_t s_full[4];   // S buffer u of consumer group g written: index 2 g + u
-    uint64_t p_full[2];   // P of group g written (one arrival per active softmax thread)
-    uint64_t p_free[2];   // PV product of group g done
+    uint64_t s_full[4];   // S buffer u of consumer group g written: index 2 g + u (256 rows: g)
+    uint64_t s_free[2];   // 256 rows: block g's S loaded by its softmax warps (one arrival per warp)
+    // P of group g written (one arrival per active softmax thread); 256 rows:
+    // P buffer 2 g + u of block g written, so that a barrier's next phase (two
+    // tiles on) cannot complete before the MMA issuer has seen this one
+    uint64_t p_full[4];
+    uint64_t p_free[4];   // PV product of group g done (256 rows: of block g from P buffer 2 g + u)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -178,9 +194,10 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mbar_init(&bars->kv_empty[i], 1);
         }
         for (int u = 0; u < 4; ++u) mbar_init(&bars->s_full[u], 1);
-        for (int gr = 0; gr < 2; ++gr) {
-            mbar_init(&bars->p_full[gr], L::kGroupThreads);
-            mbar_init(&bars->p_free[gr], 1);
+        for (int gr = 0; gr < 2; ++gr) mbar_init(&bars->s_free[gr], L::kActiveQuadrants);
+        for (int u = 0; u < 4; ++u) {
+            mbar_init(&bars->p_full[u], L::kGroupThreads);
+            mbar_init(&bars->p_free[u], 1);
         }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -205,7 +222,9 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             p.part_first[sp0.b * p.Hkv + g] = slot_idx;
         }
     }
+    tc_fence_before();   // the TMEM allocation above, before its address is read
     __syncthreads();
+    tc_fence_after();
 
     // Tiles of this split: the history [0, P) of sequence b in 64-key tiles,
     // shared out evenly over its S_b splits; the last split also takes the n_q
@@ -224,9 +243,35 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int n = has_work ? n_hist + (spec_here ? 1 : 0) : 0;
     const int64_t slot = ((int64_t)g * p.nparts + slot_idx) * p.R;   // this CTA's partial rows
 
-    // Q rows of the group into shared memory (K-major, 128-byte swizzle);
-    // rows >= R are zero.
-    if (tid < ROWS && n > 0) {
+    if constexpr (L::kRowGroups) {
+        // Q rows of the CTA into tensor memory: softmax warp w writes the rows
+        // of its lane quadrant of block w / 4 (K-major, two elements per
+        // column); rows >= R are zero.
+        if (warp < kSoftmaxWarps && n > 0) {
+            const int q4 = warp & 3, gr = warp >> 2;
+            const int rr = gr * 128 + q4 * 32 + lane;
+            const uint4* src = nullptr;
+            if (rr < Rb)
+                src = reinterpret_cast<const uint4*>(
+                    static_cast<const __nv_bfloat16*>(p.Q) +
+                    (((int64_t)b * p.Hq + (int64_t)g * p.G) * p.n_q + r0 + rr) * kD);
+            const uint32_t qaddr = bars->tmem_base + ((uint32_t)(q4 * 32) << 16) + kTmemQ +
+                                   (uint32_t)(gr * (kD / 2));
+#pragma unroll
+            for (int h = 0; h < kD / 64; ++h) {   // 64 elements = 32 columns at a time
+                uint32_t w[32];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 v = src ? src[h * 8 + j] : make_uint4(0, 0, 0, 0);
+                    w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+                }
+                tmem_st32(qaddr + (uint32_t)(32 * h), w);
+            }
+            tmem_wait_st();
+        }
+    } else if (tid < ROWS && n > 0) {
+        // Q rows of the group into shared memory (K-major, 128-byte swizzle);
+        // rows >= R are zero.
         const int r = tid;
         constexpr int kQChunks = kD / 8;   // 16-byte pieces of a Q row
         uint4 chunk[kQChunks];
@@ -332,14 +377,15 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 // their products are issued in pairs, one K step of each
                 // block in turn: successive MMAs into the same accumulator
                 // wait for each other in the tensor pipe, MMAs into the
-                // other block's accumulator do not.  S_j of both blocks
-                // goes to buffer j & 1, free once the PV pair of tile j - 2
-                // was issued; tile j's ring slot is released after its PV pair.
+                // other block's accumulator do not.  S_j (A = Q from tensor
+                // memory) goes to the block's one S buffer once its softmax
+                // warps have loaded S_{j-1}; PV_i reads P buffer i & 1 of the
+                // block; tile i's ring slot is released after its PV pair.
                 int ns = 0, npv = 0;
                 while (npv < n) {
                     bool progressed = false;
-                    if (npv < ns && mbar_try_wait(&bars->p_full[0], npv & 1) &&
-                        mbar_try_wait(&bars->p_full[1], npv & 1)) {
+                    if (npv < ns && mbar_try_wait(&bars->p_full[npv & 1], (npv >> 1) & 1) &&
+                        mbar_try_wait(&bars->p_full[2 + (npv & 1)], (npv >> 1) & 1)) {
                         tc_fence_after();
                         const int i = npv;
                         const int st = i % kStages;
@@ -349,33 +395,34 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 #pragma unroll
                             for (int u = 0; u < 2; ++u)
                                 mma_bf16(tmem + kTmemO + (uint32_t)(u * kD),
-                                         pd0 + (uint64_t)(u * (kPBytes >> 4) + k * 2),
+                                         pd0 + (uint64_t)((2 * u + (i & 1)) * (kPBytes >> 4) + k * 2),
                                          vd + (uint64_t)(k * (2048 >> 4)), L::kIdescPV,
                                          (i > 0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(&bars->p_free[0]);
-                        mma_commit(&bars->p_free[1]);
+                        mma_commit(&bars->p_free[i & 1]);
+                        mma_commit(&bars->p_free[2 + (i & 1)]);
                         mma_commit(&bars->kv_empty[st]);
                         ++npv;
                         progressed = true;
                     }
-                    if (ns < n && ns <= npv + 1 &&
+                    if (ns < n &&
+                        (ns == 0 || (mbar_try_wait(&bars->s_free[0], (ns - 1) & 1) &&
+                                     mbar_try_wait(&bars->s_free[1], (ns - 1) & 1))) &&
                         mbar_try_wait(&bars->kv_full[ns % kStages], (ns / kStages) & 1)) {
                         tc_fence_after();
                         const int j = ns;
                         const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
 #pragma unroll
                         for (int k = 0; k < kD / 16; ++k) {
-                            const uint64_t qoff = (uint64_t)(((k >> 2) * L::kQBlock + (k & 3) * 32) >> 4);
                             const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
 #pragma unroll
-                            for (int u = 0; u < 2; ++u)   // block u: Q rows 128 u .. + 127
-                                mma_bf16(tmem + kTmemS + (uint32_t)((2 * u + (j & 1)) * kKeys),
-                                         qd0 + qoff + (uint64_t)(u * ((128 * 128) >> 4)), kd + koff,
-                                         kIdescS, k > 0 ? 1u : 0u);
+                            for (int u = 0; u < 2; ++u)
+                                mma_bf16_ta(tmem + kTmemS + (uint32_t)(u * kKeys),
+                                            tmem + kTmemQ + (uint32_t)(u * (kD / 2) + 8 * k), kd + koff,
+                                            kIdescS, k > 0 ? 1u : 0u);
                         }
-                        mma_commit(&bars->s_full[j & 1]);
-                        mma_commit(&bars->s_full[2 + (j & 1)]);
+                        mma_commit(&bars->s_full[0]);
+                        mma_commit(&bars->s_full[1]);
                         ++ns;
                         progressed = true;
                     }
@@ -384,13 +431,19 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                     } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
                         if (npv < ns) {
                             // a PV pair is next: wait for the block that is not there yet
-                            if (mbar_try_wait(&bars->p_full[0], npv & 1))
-                                (void)mbar_try_wait_sleep(&bars->p_full[1], npv & 1, 500u);
+                            const uint32_t par = (uint32_t)((npv >> 1) & 1);
+                            if (mbar_try_wait(&bars->p_full[npv & 1], par))
+                                (void)mbar_try_wait_sleep(&bars->p_full[2 + (npv & 1)], par, 500u);
                             else
-                                (void)mbar_try_wait_sleep(&bars->p_full[0], npv & 1, 500u);
+                                (void)mbar_try_wait_sleep(&bars->p_full[npv & 1], par, 500u);
                         } else if (ns < n) {
-                            (void)mbar_try_wait_sleep(&bars->kv_full[ns % kStages], (ns / kStages) & 1,
-                                                      500u);
+                            if (ns > 0 && !mbar_try_wait(&bars->s_free[0], (ns - 1) & 1))
+                                (void)mbar_try_wait_sleep(&bars->s_free[0], (ns - 1) & 1, 500u);
+                            else if (ns > 0 && !mbar_try_wait(&bars->s_free[1], (ns - 1) & 1))
+                                (void)mbar_try_wait_sleep(&bars->s_free[1], (ns - 1) & 1, 500u);
+                            else
+                                (void)mbar_try_wait_sleep(&bars->kv_full[ns % kStages],
+                                                          (ns / kStages) & 1, 500u);
                         }
                     } else {
                         atomicOr(p.err, kErrWaitTimeout);
@@ -488,22 +541,58 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 spec_bits |= (vis ? 1ull : 0ull) << j;
             }
         }
+        // A warp whose 32 rows all lie past the CTA's rows computes nothing:
+        // it only keeps its place in the barrier protocol.
+        const bool idle_warp = rr - lane >= Rb;
         float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
         int k_local = 0;
         constexpr int kStep = L::kRowGroups ? 1 : 2;
         for (int i = L::kRowGroups ? 0 : gr; i < n; i += kStep, ++k_local) {
-            const int sbuf = 2 * gr + (k_local & 1);
+            // 256 rows: one S buffer per block, every phase a tile
+            const int sbuf = L::kRowGroups ? gr : 2 * gr + (k_local & 1);
+            const uint32_t s_par = L::kRowGroups ? (uint32_t)(k_local & 1) : (uint32_t)((k_local >> 1) & 1);
             const uint32_t s_col = kTmemS + (uint32_t)(sbuf * kKeys);
             ok = __all_sync(0xffffffffu,
-                            mbar_wait_sleep(&bars->s_full[sbuf], (k_local >> 1) & 1, p.err,
+                            mbar_wait_sleep(&bars->s_full[sbuf], s_par, p.err,
                                             kRoleSoftmax | kBarSFull | (unsigned)(i & 0xffff)));
             if (!ok) break;
+            if (idle_warp) {
+                if constexpr (L::kRowGroups) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->s_free[gr]);
+                    // the live warps' order: P buffer k & 1 is handed over
+                    // again only after PV_{k-2} has read it
+                    if (k_local >= 2) {
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait_sleep(&bars->p_free[2 * gr + (k_local & 1)],
+                                                        (uint32_t)(((k_local >> 1) - 1) & 1), p.err,
+                                                        kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff)));
+                        if (!ok) break;
+                    }
+                    mbar_arrive(&bars->p_full[2 * gr + (k_local & 1)]);
+                } else {
+                    // stay in step with the group's live warps: the next
+                    // tile's arrivals must not count for this one
+                    mbar_arrive(&bars->p_full[gr]);
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait_sleep(&bars->p_full[gr], (uint32_t)(k_local & 1), p.err,
+                                                    kRoleSoftmax | kBarPFull | (unsigned)(i & 0xffff)));
+                    if (!ok) break;
+                }
+                continue;
+            }
             tc_fence_after();
             uint32_t sr[2][32];
             tmem_ld32(lane_addr + s_col, sr[0]);
             tmem_ld32(lane_addr + s_col + 32, sr[1]);
             tmem_wait_ld();
+            if constexpr (L::kRowGroups) {
+                // S is in registers: the block's next S may overwrite the buffer
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->s_free[gr]);
+            }
             uint64_t valid;
             if (i < n_hist) {
                 const int64_t nv = key_end - (int64_t)(t_begin + i) * kKeys;
@@ -512,19 +601,34 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 valid = spec_bits;
             }
             float sv[64];
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            float mt;
+            if (valid == ~0ull) {
+                // a whole history tile: no mask to apply
+                float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+                for (int j = 0; j < 64; j += 4) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    sv[j + u] = ((valid >> (j + u)) & 1ull) ? __uint_as_float(sr[(j + u) >> 5][(j + u) & 31])
-                                                           : -INFINITY;
-                mx0 = fmaxf(mx0, sv[j]);
-                mx1 = fmaxf(mx1, sv[j + 1]);
-                mx2 = fmaxf(mx2, sv[j + 2]);
-                mx3 = fmaxf(mx3, sv[j + 3]);
+                    for (int u = 0; u < 4; ++u) sv[j + u] = __uint_as_float(sr[(j + u) >> 5][(j + u) & 31]);
+                    mx0 = fmax3(mx0, sv[j], sv[j + 1]);
+                    mx1 = fmax3(mx1, sv[j + 2], sv[j + 3]);
+                }
+                mt = fmaxf(mx0, mx1) * c;
+            } else {
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        sv[j + u] = ((valid >> (j + u)) & 1ull)
+                                        ? __uint_as_float(sr[(j + u) >> 5][(j + u) & 31])
+                                        : -INFINITY;
+                    mx0 = fmaxf(mx0, sv[j]);
+                    mx1 = fmaxf(mx1, sv[j + 1]);
+                    mx2 = fmaxf(mx2, sv[j + 2]);
+                    mx3 = fmaxf(mx3, sv[j + 3]);
+                }
+                mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
             }
-            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
             float corr = 1.f;
             bool rescale = false;
             if (mt > m_run + 8.f) {               // also true for the first finite tile
@@ -536,28 +640,50 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             // mask hides every key from it, with no history before it) keeps
             // p = 0 instead of exp(-inf + inf)
             const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            // packed f32x2 arithmetic: the same per-lane fma and adds, half the instructions
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
+            float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float p0 = ex2(fmaf(sv[2 * j], c, neg_m));
-                const float p1 = ex2(fmaf(sv[2 * j + 1], c, neg_m));
-                const float p2 = ex2(fmaf(sv[2 * j + 2], c, neg_m));
-                const float p3 = ex2(fmaf(sv[2 * j + 3], c, neg_m));
-                s0 += p0; s1 += p1; s2 += p2; s3 += p3;
-                pk[j] = pack_bf16x2(p0, p1);
-                pk[j + 1] = pack_bf16x2(p2, p3);
+                const float2 x01 = fma2(make_float2(sv[2 * j], sv[2 * j + 1]), c2, nm2);
+                const float2 x23 = fma2(make_float2(sv[2 * j + 2], sv[2 * j + 3]), c2, nm2);
+                const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+                const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+                s01 = add2(s01, p01);
+                s23 = add2(s23, p23);
+                pk[j] = pack_bf16x2(p01.x, p01.y);
+                pk[j + 1] = pack_bf16x2(p23.x, p23.y);
             }
-            l_run = l_run * corr + ((s0 + s1) + (s2 + s3));
-            // the previous PV of this group read P and accumulated into O
-            if (k_local > 0) {
+            l_run = l_run * corr + ((s01.x + s01.y) + (s23.x + s23.y));
+            const bool any_rescale = __any_sync(0xffffffffu, rescale);
+            if constexpr (L::kRowGroups) {
+                // P buffer k & 1 was last read by PV_{k-2}; rescaling O also
+                // needs PV_{k-1} to have accumulated into it
+                if (k_local >= 2) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait_sleep(&bars->p_free[2 * gr + (k_local & 1)],
+                                                    (uint32_t)(((k_local >> 1) - 1) & 1), p.err,
+                                                    kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff)));
+                    if (!ok) break;
+                }
+                if (any_rescale) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait_sleep(&bars->p_free[2 * gr + ((k_local - 1) & 1)],
+                                                    (uint32_t)(((k_local - 1) >> 1) & 1), p.err,
+                                                    kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff)));
+                    if (!ok) break;
+                }
+                tc_fence_after();
+            } else if (k_local > 0) {
+                // the previous PV of this group read P and accumulated into O
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
                                                 kRoleSoftmax | kBarPFree | (unsigned)(i & 0xffff)));
                 if (!ok) break;
                 tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, rescale)) {
+            if (any_rescale) {
 #pragma unroll
                 for (int qq = 0; qq < kD / 32; ++qq) {
                     uint32_t o[32];
@@ -569,7 +695,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                 }
                 tmem_wait_st();
             }
-            uint8_t* prow = smem + kOffP + gr * kPBytes + r * 128;
+            const int pbuf = L::kRowGroups ? 2 * gr + (k_local & 1) : gr;
+            uint8_t* prow = smem + kOffP + pbuf * kPBytes + r * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
@@ -577,15 +704,19 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[gr]);
+            mbar_arrive(&bars->p_full[L::kRowGroups ? 2 * gr + (k_local & 1) : gr]);
         }
         if (tid == 0) griddep_launch_dependents();
         // Wait for this group's last PV, publish (m, l), then combine both
         // groups' O columns: warp w writes columns 64 (w / 4) .. + 63 of its rows.
-        if (ok && k_local > 0)
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait_sleep(&bars->p_free[gr], (k_local - 1) & 1, p.err,
-                                            kRoleSoftmax | kBarPFree | 0xffffu));
+        if (ok && k_local > 0) {
+            // 256 rows: the block's last PV read P buffer (k - 1) & 1
+            const int fb = L::kRowGroups ? 2 * gr + ((k_local - 1) & 1) : gr;
+            const uint32_t fpar = L::kRowGroups ? (uint32_t)(((k_local - 1) >> 1) & 1)
+                                                : (uint32_t)((k_local - 1) & 1);
+            ok = __all_sync(0xffffffffu, mbar_wait_sleep(&bars->p_free[fb], fpar, p.err,
+                                                         kRoleSoftmax | kBarPFree | 0xffffu));
+        }
         if constexpr (L::kRowGroups) {
             // Each group owns its rows' partial: (O, m, l) as they stand.
             if (ok) {

@@ -34,6 +34,18 @@ RAPID_DEVICE void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t ide
         : "memory");
 }
 
+// The same product with A read from tensor memory (K-major: row m of A in
+// lane m, two 16-bit elements per 32-bit column, K step k at column + 8 k).
+RAPID_DEVICE void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 RAPID_DEVICE void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
