@@ -9,7 +9,7 @@
 // group's G * n_q query rows form the M = 128 operand of one tcgen05 MMA, so
 // every K/V byte is read from HBM once per group.
 //
-// CTA = (split s, sequence b * Hkv + KV head g); 352 threads:
+// CTA = (split s, sequence b * Hkv + KV head g); 384 threads:
 //   warps 0-7  softmax, in two consumer groups (warps 0-3 take the even
 //              tiles of the split, warps 4-7 the odd ones; in a 256-row CTA
 //              they are its two 128-row blocks and both take every tile);
@@ -23,7 +23,7 @@
 //              the group has more than 64 query rows); the
 //              last split also loads the n_q speculative rows as one more
 //              tile, which the softmax masks with the chain / tree mask.
-//   warp 10    allocates TMEM and issues the MMAs (one thread), in the order
+//   warp 11    allocates TMEM and issues the MMAs (one thread), in the order
 //              their inputs become ready: S_j = Q K_j^T (M128 N64 K128, two S
 //              buffers per group, so S runs a tile ahead of the softmax) and
 //              O_g += P_i V_i (M128 N128 K64).
@@ -43,11 +43,16 @@ namespace rapid {
 namespace {
 
 constexpr int kSoftmaxWarps = 8;                // two groups x four TMEM lane quadrants
-// The producer runs on SM sub-partition 0 (warp 8); warp 9 is idle so that the
-// MMA issuer (warp 10) sits on sub-partition 2, away from the producer.
+// Warp w runs on SM sub-partition w % 4, and the MMA issuer gets its issue
+// slots only between those of the softmax warps on its sub-partition: two busy
+// softmax warps beside it slow the tensor pipe's work by a quarter.  So the
+// issuer is warp 11, on the sub-partition of TMEM lane quadrant 3 (group rows
+// 96..127), whose softmax warps are most often idle: padding rows of a 224-row
+// tree group's second block, of an 88-row group, and absent below 97 rows.
+// The producer runs on sub-partition 0 (warp 8); warps 9 and 10 are idle.
 constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 2;
-constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int kMmaWarp = kSoftmaxWarps + 3;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
 constexpr int kKeys = 64;                       // keys per K/V tile
 constexpr int kBlockBytes = kKeys * 128;        // one 64-column block of a K or V tile (8 KB)
 constexpr int kMaxStages = 12;
@@ -373,17 +378,41 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             bool ok = true;
             uint64_t t_last = global_timer_ns();
             if constexpr (L::kRowGroups) {
-                // The two row blocks move through the tiles together, and
-                // their products are issued in pairs, one K step of each
-                // block in turn: successive MMAs into the same accumulator
-                // wait for each other in the tensor pipe, MMAs into the
-                // other block's accumulator do not.  S_j (A = Q from tensor
-                // memory) goes to the block's one S buffer once its softmax
-                // warps have loaded S_{j-1}; PV_i reads P buffer i & 1 of the
+                // The two row blocks move through the tiles together, their
+                // products issued in pairs.  S_j (A = Q from tensor memory)
+                // goes to the block's one S buffer once its softmax warps
+                // have loaded S_{j-1}; PV_i reads P buffer i & 1 of the
                 // block; tile i's ring slot is released after its PV pair.
                 int ns = 0, npv = 0;
                 while (npv < n) {
                     bool progressed = false;
+                    // S before PV: the softmax warps wait on S_j now, while
+                    // PV_{j-2} is needed only when they write P_j at the
+                    // end of the tile.
+                    if (ns < n &&
+                        (ns == 0 || (mbar_try_wait(&bars->s_free[0], (ns - 1) & 1) &&
+                                     mbar_try_wait(&bars->s_free[1], (ns - 1) & 1))) &&
+                        mbar_try_wait(&bars->kv_full[ns % kStages], (ns / kStages) & 1)) {
+                        tc_fence_after();
+                        const int j = ns;
+                        const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
+                        // one block's K steps back to back: consecutive MMAs
+                        // into one accumulator run at the tensor pipe's rate,
+                        // alternating between two accumulators at half of it
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+                            for (int k = 0; k < kD / 16; ++k) {
+                                const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
+                                mma_bf16_ta(tmem + kTmemS + (uint32_t)(u * kKeys),
+                                            tmem + kTmemQ + (uint32_t)(u * (kD / 2) + 8 * k), kd + koff,
+                                            kIdescS, k > 0 ? 1u : 0u);
+                            }
+                            mma_commit(&bars->s_full[u]);
+                        }
+                        ++ns;
+                        progressed = true;
+                    }
                     if (npv < ns && mbar_try_wait(&bars->p_full[npv & 1], (npv >> 1) & 1) &&
                         mbar_try_wait(&bars->p_full[2 + (npv & 1)], (npv >> 1) & 1)) {
                         tc_fence_after();
@@ -405,45 +434,29 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                         ++npv;
                         progressed = true;
                     }
-                    if (ns < n &&
-                        (ns == 0 || (mbar_try_wait(&bars->s_free[0], (ns - 1) & 1) &&
-                                     mbar_try_wait(&bars->s_free[1], (ns - 1) & 1))) &&
-                        mbar_try_wait(&bars->kv_full[ns % kStages], (ns / kStages) & 1)) {
-                        tc_fence_after();
-                        const int j = ns;
-                        const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
-#pragma unroll
-                        for (int k = 0; k < kD / 16; ++k) {
-                            const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
-#pragma unroll
-                            for (int u = 0; u < 2; ++u)
-                                mma_bf16_ta(tmem + kTmemS + (uint32_t)(u * kKeys),
-                                            tmem + kTmemQ + (uint32_t)(u * (kD / 2) + 8 * k), kd + koff,
-                                            kIdescS, k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars->s_full[0]);
-                        mma_commit(&bars->s_full[1]);
-                        ++ns;
-                        progressed = true;
-                    }
                     if (progressed) {
                         t_last = global_timer_ns();
                     } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
-                        if (npv < ns) {
-                            // a PV pair is next: wait for the block that is not there yet
-                            const uint32_t par = (uint32_t)((npv >> 1) & 1);
-                            if (mbar_try_wait(&bars->p_full[npv & 1], par))
-                                (void)mbar_try_wait_sleep(&bars->p_full[2 + (npv & 1)], par, 500u);
-                            else
-                                (void)mbar_try_wait_sleep(&bars->p_full[npv & 1], par, 500u);
-                        } else if (ns < n) {
+                        // Sleep on the event due first.  Within a tile the
+                        // softmax warps release S as soon as they have loaded
+                        // it and hand over P only at the end, so while the
+                        // next S pair may be issued (at most one ahead of the
+                        // PV pairs) its inputs come before the pending P.
+                        if (ns < n && ns <= npv + 1) {
                             if (ns > 0 && !mbar_try_wait(&bars->s_free[0], (ns - 1) & 1))
                                 (void)mbar_try_wait_sleep(&bars->s_free[0], (ns - 1) & 1, 500u);
                             else if (ns > 0 && !mbar_try_wait(&bars->s_free[1], (ns - 1) & 1))
                                 (void)mbar_try_wait_sleep(&bars->s_free[1], (ns - 1) & 1, 500u);
                             else
                                 (void)mbar_try_wait_sleep(&bars->kv_full[ns % kStages],
-                                                          (ns / kStages) & 1, 500u);
+                                                          (ns / kStages) & 1, 200u);
+                        } else if (npv < ns) {
+                            // a PV pair is next: wait for the block that is not there yet
+                            const uint32_t par = (uint32_t)((npv >> 1) & 1);
+                            if (mbar_try_wait(&bars->p_full[npv & 1], par))
+                                (void)mbar_try_wait_sleep(&bars->p_full[2 + (npv & 1)], par, 500u);
+                            else
+                                (void)mbar_try_wait_sleep(&bars->p_full[npv & 1], par, 500u);
                         }
                     } else {
                         atomicOr(p.err, kErrWaitTimeout);
