@@ -87,7 +87,8 @@ constexpr int kGT = kRT / kGroups;       // threads of a group
 constexpr int kGW = kGT / 32;            // warps of a group
 
 struct RowsShared {
-    uint64_t full[kGroups];   // the group's (z, q) slice landed
+    uint64_t zfull[kGroups];  // the z half of the group's slice landed (pass 1 needs only z)
+    uint64_t full[kGroups];   // the q half landed
     uint64_t mb1[kGroups];    // slice partials of reduction 1 received
     uint64_t mb2[kGroups];    // slice partials of reduction 2 received
     uint64_t stagger;         // group 0 is past its first reduction 1: group 1 may start
@@ -333,6 +334,7 @@ accept_rows_kernel(const AcceptParams p) {
 
     if (t == 0) {
         for (int i = 0; i < kGroups; ++i) {
+            mbar_init(&sh.zfull[i], 1);
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.mb1[i], 1);
             mbar_init(&sh.mb2[i], 1);
@@ -374,14 +376,15 @@ accept_rows_kernel(const AcceptParams p) {
         return i;
     };
     auto load_row = [&](int i) {      // one thread, bulk path, a row that is not padding
-        mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 8));
+        mbar_arrive_expect_tx(&sh.zfull[g], (uint32_t)(n * 4));
+        mbar_arrive_expect_tx(&sh.full[g], (uint32_t)(n * 4));
         if (n > 0) {
             // rows are read once here (the selection re-reads at most one row
             // of a sequence, which it prefetches itself): evict-first, so the
             // stream does not push the selection's code and inputs out of L2
             const int64_t off = row_of(i) * p.V + lo;
             const uint64_t pol = l2_policy_evict_first();
-            bulk_g2s_hint(zb, p.z + off, (uint32_t)(n * 4), &sh.full[g], pol);
+            bulk_g2s_hint(zb, p.z + off, (uint32_t)(n * 4), &sh.zfull[g], pol);
             bulk_g2s_hint(qb, p.q + off, (uint32_t)(n * 4), &sh.full[g], pol);
         }
     };
@@ -419,8 +422,8 @@ accept_rows_kernel(const AcceptParams p) {
     // independently; the last warp of a phase combines the group's partials
     // and sends them to the cluster, and every warp waits for the cluster's
     // partials itself.  The other group computes while this one waits.
-    // kx counts the group's rows that are not padding: the phase of full[g],
-    // mb1[g] and mb2[g] for the row at hand.
+    // kx counts the group's rows that are not padding: the phase of zfull[g],
+    // full[g], mb1[g] and mb2[g] for the row at hand.
     int kx = 0;
 #pragma unroll 1
     for (int i = g; i < nrows; i += 2) {
@@ -446,7 +449,8 @@ accept_rows_kernel(const AcceptParams p) {
         if (i == 1)
             wait_or_abort(&sh.stagger, 0u, &sh.abort, p.err, 0x06000000u);
         if (p.bulk) {
-            wait_or_abort(&sh.full[g], (uint32_t)(kx & 1), &sh.abort, p.err,
+            // pass 1 reads only z; q keeps landing meanwhile
+            wait_or_abort(&sh.zfull[g], (uint32_t)(kx & 1), &sh.abort, p.err,
                           0x01000000u | (unsigned)(i & 0xffff));
         } else {
             const int64_t off = row * p.V + lo;
@@ -456,7 +460,8 @@ accept_rows_kernel(const AcceptParams p) {
             }
             group_sync(g);
         }
-        // z and q at the token of child c of this row, for its ratio test
+        // z and q at the token of child c of this row, for its ratio test (q
+        // once its half has landed, before pass 2)
         int key = -1;
         float2 zq = make_float2(0.f, 0.f);
         if (rt_thread && c > j && my_par == j) {
@@ -464,7 +469,7 @@ accept_rows_kernel(const AcceptParams p) {
                 key = rank == 0 ? -2 : -1;
             } else if (my_tok >= lo && my_tok < lo + n) {
                 key = my_tok;
-                zq = make_float2(zb[my_tok - lo], qb[my_tok - lo]);
+                zq.x = zb[my_tok - lo];
             }
         }
         // pass 1; the group's last warp sends the slice's (m, s) to the cluster
@@ -496,6 +501,10 @@ accept_rows_kernel(const AcceptParams p) {
             st.s1 = r1.s;
         }
         if (i == 0 && tg == 0) mbar_arrive(&sh.stagger);
+        if (p.bulk)
+            wait_or_abort(&sh.full[g], (uint32_t)(kx & 1), &sh.abort, p.err,
+                          0x04000000u | (unsigned)(i & 0xffff));
+        if (key >= 0) zq.y = qb[key - lo];
         // pass 2; the group's last warp sends the slice's (reference, s, max a)
         {
             float amw;
@@ -573,7 +582,10 @@ accept_rows_kernel(const AcceptParams p) {
             for (int gg = 0; gg < kGroups; ++gg) {
                 int nmine = 0;   // the group's real rows: one buffer phase each
                 for (int i = gg; i < nrows; i += 2) nmine += padding(i) ? 0 : 1;
-                if (nmine > 0) mbar_wait(&sh.full[gg], (uint32_t)((nmine - 1) & 1), nullptr);
+                if (nmine > 0) {
+                    mbar_wait(&sh.zfull[gg], (uint32_t)((nmine - 1) & 1), nullptr);
+                    mbar_wait(&sh.full[gg], (uint32_t)((nmine - 1) & 1), nullptr);
+                }
             }
         }
     }
