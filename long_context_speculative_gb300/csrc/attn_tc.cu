@@ -24,9 +24,10 @@
 //              last split also loads the n_q speculative rows as one more
 //              tile, which the softmax masks with the chain / tree mask.
 //   warp 11    allocates TMEM and issues the MMAs (one thread), in the order
-//              their inputs become ready: S_j = Q K_j^T (M128 N64 K128, two S
-//              buffers per group, so S runs a tile ahead of the softmax) and
-//              O_g += P_i V_i (M128 N128 K64).
+//              their inputs become ready: S_j = Q K_j^T (M128 N64 K = d, two S
+//              buffers per group, so S runs a tile ahead of the softmax; in a
+//              256-row CTA one per block, released as soon as it is loaded)
+//              and O_g += P_i V_i (M128 N = d K64).
 // Shared-memory operands use the 128-byte swizzle; Q, K and P are K-major,
 // V is MN-major (d contiguous).  Every mbarrier wait is bounded in wall-clock
 // time; on a timeout the kernel records an error code, stops issuing work,
@@ -363,10 +364,8 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------ MMA issuer ----------------------------
-        // Issues S_j = Q K_j^T and O_g += P_i V_i in the order their inputs
-        // become ready: S_j needs K/V tile j and its S buffer (group j & 1,
-        // buffer (j >> 1) & 1), which is free once P of tile j - 4 was handed
-        // over, i.e. j <= next_pv + 3; PV_i needs P of tile i.
+        // Issues S_j = Q K_j^T and O += P_i V_i in the order their inputs
+        // become ready (one loop per configuration below).
         if (lane == 0) {
             // Descriptors are built once; the one of a later operand block is
             // the base plus its byte offset in 16-byte units (all shared
@@ -467,64 +466,68 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                     }
                 }
             } else {
-            int next_s = 0, next_pv = 0;
-            while (next_pv < n) {
-                bool progressed = false;
-                if (next_s < n && next_s <= next_pv + 3 &&
-                    mbar_try_wait(&bars->kv_full[next_s % kStages], (next_s / kStages) & 1)) {
-                    tc_fence_after();
-                    const int j = next_s;
-                    const int sbuf = 2 * (j & 1) + ((j >> 1) & 1);
-                    const uint32_t dS = tmem + kTmemS + (uint32_t)(sbuf * kKeys);
-                    const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
+                // Issues S_j and PV_i in the order their inputs become ready:
+                // S_j needs K/V tile j and its S buffer (group j & 1, buffer
+                // (j >> 1) & 1), free once P of tile j - 4 was handed over, i.e.
+                // j <= next_pv + 3; PV_i needs P of tile i.
+                int next_s = 0, next_pv = 0;
+                while (next_pv < n) {
+                    bool progressed = false;
+                    if (next_s < n && next_s <= next_pv + 3 &&
+                        mbar_try_wait(&bars->kv_full[next_s % kStages], (next_s / kStages) & 1)) {
+                        tc_fence_after();
+                        const int j = next_s;
+                        const int sbuf = 2 * (j & 1) + ((j >> 1) & 1);
+                        const uint32_t dS = tmem + kTmemS + (uint32_t)(sbuf * kKeys);
+                        const uint64_t kd = kd0 + (uint64_t)((j % kStages) * (kStageBytes >> 4));
 #pragma unroll
-                    for (int k = 0; k < kD / 16; ++k) {
-                        const uint64_t qoff = (uint64_t)(((k >> 2) * L::kQBlock + (k & 3) * 32) >> 4);
-                        const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
-                        mma_bf16(dS, qd0 + qoff, kd + koff, kIdescS, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint64_t qoff = (uint64_t)(((k >> 2) * L::kQBlock + (k & 3) * 32) >> 4);
+                            const uint64_t koff = (uint64_t)(((k >> 2) * (kKeys * 128) + (k & 3) * 32) >> 4);
+                            mma_bf16(dS, qd0 + qoff, kd + koff, kIdescS, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->s_full[sbuf]);
+                        ++next_s;
+                        progressed = true;
                     }
-                    mma_commit(&bars->s_full[sbuf]);
-                    ++next_s;
-                    progressed = true;
-                }
-                if (next_pv < next_s &&
-                    mbar_try_wait(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-                    tc_fence_after();
-                    const int i = next_pv;
-                    const int gr = i & 1;
-                    const int st = i % kStages;
-                    const uint64_t pd = pd0 + (uint64_t)(gr * (kPBytes >> 4));
-                    const uint64_t vd = vd0 + (uint64_t)(st * (kStageBytes >> 4));
-                    const uint32_t dO = tmem + kTmemO + (uint32_t)(gr * kD);
+                    if (next_pv < next_s &&
+                        mbar_try_wait(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                        tc_fence_after();
+                        const int i = next_pv;
+                        const int gr = i & 1;
+                        const int st = i % kStages;
+                        const uint64_t pd = pd0 + (uint64_t)(gr * (kPBytes >> 4));
+                        const uint64_t vd = vd0 + (uint64_t)(st * (kStageBytes >> 4));
+                        const uint32_t dO = tmem + kTmemO + (uint32_t)(gr * kD);
 #pragma unroll
-                    for (int k = 0; k < kKeys / 16; ++k) {
-                        mma_bf16(dO, pd + (uint64_t)(k * 2), vd + (uint64_t)(k * (2048 >> 4)),
-                                 L::kIdescPV, (i > 1 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kKeys / 16; ++k) {
+                            mma_bf16(dO, pd + (uint64_t)(k * 2), vd + (uint64_t)(k * (2048 >> 4)),
+                                     L::kIdescPV, (i > 1 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars->p_free[gr]);
+                        mma_commit(&bars->kv_empty[st]);
+                        ++next_pv;
+                        progressed = true;
                     }
-                    mma_commit(&bars->p_free[gr]);
-                    mma_commit(&bars->kv_empty[st]);
-                    ++next_pv;
-                    progressed = true;
+                    if (progressed) {
+                        t_last = global_timer_ns();
+                    } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
+                        // Nothing ready: suspend on the barrier whose completion
+                        // unblocks the most (a pending PV first); the thread
+                        // wakes as soon as that phase completes.
+                        if (next_pv < next_s)
+                            (void)mbar_try_wait_sleep(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1, 500u);
+                        else if (next_s < n)
+                            (void)mbar_try_wait_sleep(&bars->kv_full[next_s % kStages],
+                                                      (next_s / kStages) & 1, 500u);
+                    } else {
+                        atomicOr(p.err, kErrWaitTimeout);
+                        atomicCAS(p.err + 1, 0u,
+                                  0x80000000u | kRoleMma | kBarPFull | (unsigned)(next_pv & 0xffff));
+                        ok = false;
+                        break;
+                    }
                 }
-                if (progressed) {
-                    t_last = global_timer_ns();
-                } else if (global_timer_ns() - t_last <= kWaitLimitNs) {
-                    // Nothing ready: suspend on the barrier whose completion
-                    // unblocks the most (a pending PV first); the thread
-                    // wakes as soon as that phase completes.
-                    if (next_pv < next_s)
-                        (void)mbar_try_wait_sleep(&bars->p_full[next_pv & 1], (next_pv >> 1) & 1, 500u);
-                    else if (next_s < n)
-                        (void)mbar_try_wait_sleep(&bars->kv_full[next_s % kStages],
-                                                  (next_s / kStages) & 1, 500u);
-                } else {
-                    atomicOr(p.err, kErrWaitTimeout);
-                    atomicCAS(p.err + 1, 0u,
-                              0x80000000u | kRoleMma | kBarPFull | (unsigned)(next_pv & 0xffff));
-                    ok = false;
-                    break;
-                }
-            }
             }
             if (!ok) bars->abort = 1;
             // drain: every MMA issued so far has completed once this arrives
