@@ -85,11 +85,12 @@ def test_group_widths(G, n_q, d):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False),
-                                        (16, 20, True), (8, 64, False)])
+                                        (16, 20, True), (8, 64, False), (257, 1, False), (5, 52, True)])
 def test_pair_widths_ragged(G, n_q, tree, d):
     # 129..256 group rows run as one CTA whose two 128-row blocks take every
-    # K/V tile; 257..512 as two such CTAs (320 and 512 rows here); ragged
-    # prefixes include an empty history and a single key
+    # K/V tile; 257..512 as two such CTAs (320 and 512 rows here; 257 and 260
+    # leave the second CTA one or four rows, the rest of its warps idle);
+    # ragged prefixes include an empty history and a single key
     w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=d, n_q=n_q, prefix=2100, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, tree=tree,
                     tree_nodes_max_depth=6, seed=60 + G + n_q)
