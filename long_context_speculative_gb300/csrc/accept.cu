@@ -630,6 +630,9 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     const int warp = t >> 5, lane = t & 31;
     const int n_q = p.n_q;
     griddep_wait();
+    // the next kernel of the stream may launch now: whatever it does before
+    // its own griddep_wait() touches no memory this grid reads or writes
+    griddep_launch_dependents();
     const int nn = node_count(p, b);   // nodes of this sequence
     // Device-side inputs the host cannot check (clamped or rejected on the
     // way, so memory stays safe): a node count outside [1, n_q], a parent
