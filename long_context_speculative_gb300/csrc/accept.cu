@@ -43,8 +43,13 @@ namespace {
 constexpr int kRT = kAcceptRowThreads;
 constexpr int kST = kAcceptSelThreads;
 constexpr int kSW = kST / 32;
+// float4 groups per lane run in the draw: a warp segment of a slice of at
+// most kAcceptMaxSlice entries is at most this many 128-entry blocks
+constexpr int kRunF4 = (kAcceptMaxSlice + kSW * 128 - 1) / (kSW * 128);
 constexpr size_t kSmemBudget = (size_t)2 * kAcceptMaxSlice * 8;   // dynamic shared memory for the row ring
 constexpr int kMinSlice = 1024;          // rows shorter than C x this use fewer slices
+constexpr int kSelSlice = 2048;          // selection: entries per CTA, at least
+constexpr int kSelPerSm = 3;             // selection CTAs resident per SM (its launch bounds)
 constexpr float kEtaBound = 32.f;        // largest eta for which max x + eta is the reference of a
 
 __device__ __forceinline__ float ex2(float x) {
@@ -148,6 +153,14 @@ __device__ __forceinline__ bool group_arrive(int* counter) {
     last = __shfl_sync(0xffffffffu, last, 0);
     __syncwarp();
     return last != 0;
+}
+
+// Split cluster barrier: arrive (no ordering) and wait, by every thread.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t mapa_u32(uint32_t addr, uint32_t rank) {
@@ -599,9 +612,10 @@ accept_rows_kernel(const AcceptParams p) {
 // the next token by inverse CDF in token-id order with u_{e+1}: the residual
 // max(p - p_hat, p - q, 0) if e has children (a rejection happened below it),
 // else p (the bonus draw; also the fallback when the residual has no mass).
-// The weights stay in the CTA's shared memory; the slice totals cross the
-// cluster through distributed shared memory, and the CTA whose slice holds
-// the target scans it there.
+// The weights stay in the CTA's shared memory; each CTA stores its slice
+// total into every peer's table (distributed shared memory, one cluster
+// barrier), and in the CTA whose slice holds the target one warp finds the
+// warp segment that holds it, then the entry, 128 entries at a time.
 __device__ __forceinline__ float resid_weight(float z, float qk, float invT, float eta, float m1,
                                               float inv_s1, float m2, float inv_s2, float thr) {
     const float x = z * invT;
@@ -612,16 +626,30 @@ __device__ __forceinline__ float resid_weight(float z, float qk, float invT, flo
     return pk - min3(pk, ph, qk);   // max(p - p_hat, p - q, 0)
 }
 
+// Float4 group i of the weights (entries i .. i + 3, i a multiple of 4);
+// entries at or past a1 read as 0.
+__device__ __forceinline__ float4 run_f4(const float* sw, int i, int a1) {
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i + 3 < a1) {
+        w = *reinterpret_cast<const float4*>(sw + i);
+    } else if (i < a1) {
+        w.x = sw[i];
+        if (i + 1 < a1) w.y = sw[i + 1];
+        if (i + 2 < a1) w.z = sw[i + 2];
+    }
+    return w;
+}
+
 __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParams p) {
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ float4 sel_dyn[];
     float* sw = reinterpret_cast<float*>(sel_dyn);   // [chunk] weights of this slice
     __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq], s_kids[kAcceptMaxNq];
     __shared__ int s_key[2];
-    __shared__ int s_e, s_has_children, s_owner, s_ow;
-    __shared__ float s_tin, s_tw;
-    __shared__ float s_seg[kSW];
-    __shared__ float s_total[2];   // this slice's weight total; the cluster's
+    __shared__ int s_e, s_has_children;
+    __shared__ float s_seg[kSW];   // weight total of each warp's segment
+    __shared__ float s_run[kSW][32], s_runi[kSW][32];   // lane runs of each segment: sums, inclusive prefix
+    __shared__ float s_tot[2][kAcceptMaxCluster];   // every slice's total, per round
     __shared__ float4 s_stats[kAcceptMaxNq];   // every row's (m1, s1, m2, s2), read up front
 
     const int cs = (int)cluster.block_rank();   // vocabulary slice
@@ -629,6 +657,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     const int t = threadIdx.x;
     const int warp = t >> 5, lane = t & 31;
     const int n_q = p.n_q;
+    cluster_arrive();   // this CTA has started; peers wait for it before storing into it
     griddep_wait();
     // the next kernel of the stream may launch now: whatever it does before
     // its own griddep_wait() touches no memory this grid reads or writes
@@ -669,11 +698,12 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     int key = -1;
     if (t < nn) {
         if (!s_kids[t]) {   // a leaf
-            int depth = 0;
-            for (int v = t; v != 0; v = s_par[v]) ++depth;
-            int len = depth, pos = depth;
-            for (int v = t; v != 0; v = s_par[v], --pos)
-                if (!s_acc[v]) len = pos - 1;
+            // one walk up: the depth, and the steps from the leaf to the
+            // rejected node nearest the root (the path's first rejection)
+            int steps = 0, rej = -1;
+            for (int v = t; v != 0; v = s_par[v], ++steps)
+                if (!s_acc[v]) rej = steps;
+            const int len = rej < 0 ? steps : steps - rej - 1;
             key = (len << 8) | (255 - t);   // most accepted, then smallest leaf
         }
     }
@@ -706,6 +736,13 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     __syncthreads();
 
     const int e = s_e;
+    // the uniform of the draw, u_{e+1}: warp 0 needs it after the exchange
+    float u = 0.f;
+    if (warp == 0) {
+        const uint2 key = philox_key(p);
+        const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, key.x, key.y);
+        u = word_uniform(rnd.w[1]);
+    }
     const int64_t row = (int64_t)b * n_q + e;
     const float4 sts = s_stats[e];
     const float m1 = sts.x, inv_s1 = 1.f / sts.y, m2 = sts.z, inv_s2 = 1.f / sts.w;
@@ -724,16 +761,26 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     }
 
     // The residual if e has children, else p; p also when the residual has no
-    // mass in any slice.
+    // mass in any slice.  Warp w weights one contiguous segment [g0, g1) of
+    // the slice (a multiple of 128 entries long, so float4 groups never
+    // straddle two segments); its sum is the segment's total, which the
+    // draw below uses without reading the weights again.
     bool resid = s_has_children != 0;
-    for (;;) {
+    const int seg = (n + kSW * 128 - 1) / (kSW * 128) * 128;
+    const int g0 = min(n, warp * seg);
+    const int g1 = min(n, g0 + seg);
+    const int nf = seg / 128;   // float4 groups per lane run: at most kRunF4 (slices of at most kAcceptMaxSlice)
+    int owner = -1;
+    float tin = INFINITY;
+    float segv = 0.f, segi = 0.f;   // warp 0: segment total and inclusive prefix, one per lane
+    for (int round = 0;; ++round) {
         float acc = 0.f;
         if (p.bulk) {   // 16-byte aligned rows, n a multiple of 4
             const float4* z4 = reinterpret_cast<const float4*>(zr);
             const float4* q4 = reinterpret_cast<const float4*>(qr);
             float4* w4 = reinterpret_cast<float4*>(sw);
 #pragma unroll 4
-            for (int k = t; k < n / 4; k += kST) {
+            for (int k = g0 / 4 + lane; k < g1 / 4; k += 32) {
                 const float4 a = z4[k];
                 float4 w;
                 if (resid) {
@@ -753,7 +800,7 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
             }
         } else {
 #pragma unroll 4
-            for (int k = t; k < n; k += kST) {
+            for (int k = g0 + lane; k < g1; k += 32) {
                 const float w = resid ? resid_weight(zr[k], qr[k], p.invT, p.eta, m1, inv_s1, m2,
                                                      inv_s2, thr)
                                       : ex2((zr[k] * p.invT - m1) * kLog2e) * inv_s1;
@@ -763,135 +810,132 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
         }
         acc = warp_sum(acc);
         if (lane == 0) s_seg[warp] = acc;
-        __syncthreads();
-        if (t == 0) {
-            float tot = 0.f;
-            for (int w = 0; w < kSW; ++w) tot += s_seg[w];
-            s_total[0] = tot;
-        }
-        cluster.sync();   // every slice's total is in place
-        if (warp == 0) {   // the cluster's totals, in slice order
-            const float mc = lane < p.C ? *cluster.map_shared_rank(&s_total[0], lane) : 0.f;
-            const float totals = warp_sum(mc);
-            const uint2 key = philox_key(p);
-            const Philox4 rnd = philox4x32_10((uint32_t)(e + 1), (uint32_t)b, 0u, 0u, key.x, key.y);
-            const float target = word_uniform(rnd.w[1]) * totals;
-            float incl = mc;
+        // The draw's search tables, built while the cluster waits for its
+        // slowest slice: each warp's segment in 32 contiguous lane runs of
+        // nf float4 groups (sums and inclusive prefix), and in warp 0 the
+        // segment totals with their inclusive prefix.
+        __syncwarp();
+        {
+            const int r0 = g0 + lane * 4 * nf;
+            float ls = 0.f;
+#pragma unroll
+            for (int j = 0; j < kRunF4; ++j) {
+                if (j < nf) {
+                    const float4 w = run_f4(sw, r0 + 4 * j, g1);
+                    ls = (((ls + w.x) + w.y) + w.z) + w.w;
+                }
+            }
+            float incl = ls;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            const unsigned hit = __ballot_sync(0xffffffffu, mc > 0.f && incl > target);
-            const unsigned pos = __ballot_sync(0xffffffffu, mc > 0.f);
-            int owner = -1;
-            float tin = INFINITY;
-            if (hit) {
-                owner = __ffs(hit) - 1;
-                tin = target - __shfl_sync(0xffffffffu, incl - mc, owner);
-            } else if (pos) {
-                owner = 31 - __clz(pos);   // rounding left the target past the end
-            }
-            if (lane == 0) {
-                s_owner = owner;
-                s_tin = tin;
-                s_total[1] = totals;
+            s_run[warp][lane] = ls;
+            s_runi[warp][lane] = incl;
+        }
+        __syncthreads();
+        // every CTA of the cluster has started (the arrival at entry) before
+        // warp 0 stores this slice's total into each peer's table
+        cluster_wait();
+        if (warp == 0) {
+            segv = lane < kSW ? s_seg[lane] : 0.f;
+            const float tot = warp_sum(segv);
+            if (lane < p.C) *cluster.map_shared_rank(&s_tot[round][cs], lane) = tot;
+            segi = segv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, segi, o);
+                if (lane >= o) segi += y;
             }
         }
-        cluster.sync();   // every CTA has read the totals: they may be rewritten, the CTAs may leave
-        if (!resid || s_total[1] > 0.f) break;
-        resid = false;
+        cluster.sync();   // every table holds every slice's total; nothing remote is read after this
+        // each warp reads the table: the totals, in slice order, are the same
+        // bits in every warp and every CTA, and so is the decision to go on
+        const float mc = lane < p.C ? s_tot[round][lane] : 0.f;
+        const float totals = warp_sum(mc);
+        if (resid && !(totals > 0.f)) {
+            resid = false;
+            cluster_arrive();   // pairs with the wait before the next round's stores
+            continue;
+        }
+        if (warp != 0) return;
+        const float target = u * totals;
+        float incl = mc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, mc > 0.f && incl > target);
+        const unsigned pos = __ballot_sync(0xffffffffu, mc > 0.f);
+        if (hit) {
+            owner = __ffs(hit) - 1;
+            tin = target - __shfl_sync(0xffffffffu, incl - mc, owner);
+        } else if (pos) {
+            owner = 31 - __clz(pos);   // rounding left the target past the end
+        }
+        break;
     }
-    const int owner = s_owner;
+    // warp 0 alone from here
     if (owner < 0) {   // no mass at all (degenerate input)
-        if (cs == 0 && t == 0) p.next_token[b] = 0;
+        if (cs == 0 && lane == 0) p.next_token[b] = 0;
         return;
     }
     if (cs != owner) return;
-    const float tin = s_tin;
-    // one contiguous segment per warp: its sum, then the warp whose segment holds the target
-    const int seg = (n + kSW * 32 - 1) / (kSW * 32) * 32;
-    const int g0 = warp * seg;
-    const int g1 = min(n, g0 + seg);
-    float acc = 0.f;
-    for (int k = g0 + lane; k < g1; k += 32) acc += sw[k];
-    acc = warp_sum(acc);
-    if (lane == 0) s_seg[warp] = acc;
-    __syncthreads();
-    if (warp == 0) {
-        const float v = lane < kSW ? s_seg[lane] : 0.f;
-        float incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && incl > tin);
-        const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
-        int ow = -1;
-        float tw = INFINITY;
+    // the segment that holds the target, from the segment totals
+    int ow = -1;
+    float tw = INFINITY;
+    {
+        const unsigned hit = __ballot_sync(0xffffffffu, segv > 0.f && segi > tin);
+        const unsigned pos = __ballot_sync(0xffffffffu, segv > 0.f);
         if (hit) {
             ow = __ffs(hit) - 1;
-            tw = tin - __shfl_sync(0xffffffffu, incl - v, ow);
+            tw = tin - __shfl_sync(0xffffffffu, segi - segv, ow);
         } else if (pos) {
             ow = 31 - __clz(pos);
         }
-        if (lane == 0) {
-            s_ow = ow;
-            s_tw = tw;
-        }
     }
-    __syncthreads();
-    const int ow = s_ow;
     if (ow < 0) {   // the owner slice has no mass (rounding): its first entry
-        if (t == 0) p.next_token[b] = (int)lo;
+        if (lane == 0) p.next_token[b] = (int)lo;
         return;
     }
-    if (warp == ow) {
-        // the segment in 32 contiguous runs, one per lane: run sums, the run
-        // that holds the target, then a sequential scan of that run
-        const float tw = s_tw;
-        const int per = (g1 - g0 + 31) / 32;
-        const int a0 = min(g1, g0 + lane * per);
-        const int a1 = min(g1, a0 + per);
-        float ls = 0.f;
-        for (int k = a0; k < a1; ++k) ls += sw[k];
-        float incl = ls;
+    // the run that holds the target (else, from rounding, the last run with
+    // mass), then the first positive entry of that run whose running sum
+    // passes the target, else the run's last positive entry
+    const int a0 = ow * seg;
+    const int a1 = min(n, a0 + seg);
+    const int r0 = a0 + lane * 4 * nf;
+    const float ls = s_run[ow][lane];
+    const float incl = s_runi[ow][lane];
+    const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > tw);
+    const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
+    const int src = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    if (src < 0) {   // unreachable: the segment has mass
+        if (lane == 0) p.next_token[b] = (int)(lo + a0);
+        return;
+    }
+    const float tl = tw - __shfl_sync(0xffffffffu, incl - ls, src);
+    if (lane != src) return;
+    float ce = 0.f;
+    int pick = -1, last = -1;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, ls > 0.f && incl > tw);
-        const unsigned pos = __ballot_sync(0xffffffffu, ls > 0.f);
-        int run = -1;
-        float tl = INFINITY;
-        if (hit) {
-            run = __ffs(hit) - 1;
-            tl = tw - __shfl_sync(0xffffffffu, incl - ls, run);
-        } else if (pos) {
-            run = 31 - __clz(pos);
-        }
-        if (lane == run) {
-            float ce = 0.f;
-            int kpick = -1, klast = -1;
-            for (int k = a0; k < a1; ++k) {
-                const float w = sw[k];
-                if (w > 0.f) {
-                    klast = k;
-                    if (ce + w > tl) {
-                        kpick = k;
-                        break;
-                    }
+    for (int j = 0; j < kRunF4; ++j) {
+        if (j < nf) {
+            const int i = r0 + 4 * j;
+            const float4 w = run_f4(sw, i, a1);
+            const float c[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (c[k] > 0.f) {
+                    last = i + k;
+                    if (pick < 0 && ce + c[k] > tl) pick = i + k;
                 }
-                ce += w;
+                ce += c[k];
             }
-            if (kpick < 0) kpick = klast;
-            p.next_token[b] = (int)(lo + kpick);
-        } else if (run < 0 && lane == 0) {
-            p.next_token[b] = (int)(lo + g0);   // unreachable: the segment has mass
         }
     }
+    p.next_token[b] = (int)(lo + (pick >= 0 ? pick : last));
 }
 
 template <int F>
@@ -1045,9 +1089,25 @@ cudaError_t launch_accept(const AcceptParams& p0, const AcceptShape& sh, cudaStr
     p.nbuf = sh.nbuf;
     p.rows = p.B * p.n_q;
     p.nclusters = p.rows < sh.max_clusters ? p.rows : sh.max_clusters;
-    if (p.nclusters < 1) return cudaErrorNotSupported;
+    if (p.nclusters < 1 || p.chunk > kAcceptMaxSlice) return cudaErrorNotSupported;
     cudaError_t e = launch_rows_dispatch(sh.F, p, st);
     if (e != cudaSuccess) return e;
+    // The selection slices row e on its own: one CTA per kSelSlice entries,
+    // at most kAcceptMaxCluster, so that each CTA's share of the re-read is
+    // in flight in one round of loads -- while the batch's clusters still fit
+    // in one wave (kSelPerSm CTAs per SM); larger batches keep the row
+    // kernel's slices (fewer CTAs repeating the path search).
+    int sc = (p.V + kSelSlice - 1) / kSelSlice;
+    if (sc > kAcceptMaxCluster) sc = kAcceptMaxCluster;
+    if (sc < 1) sc = 1;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if ((int64_t)p.B * sc > (int64_t)kSelPerSm * sms) sc = p.C;
+    p.C = sc;
+    p.chunk = ((p.V + sc - 1) / sc + 3) / 4 * 4;
+    if (p.chunk > kAcceptMaxSlice) return cudaErrorNotSupported;
     const size_t sel_smem = (size_t)p.chunk * 4;
     e = cudaFuncSetAttribute(accept_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sel_smem);
