@@ -61,9 +61,11 @@ def test_bf16_needle_dominated_output():
     _run_and_check(w, needle=True)
 
 
-@pytest.mark.parametrize("P", [0, 1, 127, 128, 129, 4000])
-def test_edge_prefix_lengths(P):
-    w = wl.Workload("t", B=1, Hq=4, Hkv=1, d=128, n_q=5, prefix=4000, layers=1, V=10,
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("P", [0, 1, 127, 128, 129, 191, 257, 4000])
+def test_edge_prefix_lengths(P, d):
+    # 0..5 tiles: fewer tiles than consumer groups, and each group last
+    w = wl.Workload("t", B=1, Hq=4, Hkv=1, d=d, n_q=5, prefix=4000, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, seed=31)
     _run_and_check(w, prefix_override=[P])
 
@@ -85,12 +87,15 @@ def test_group_widths(G, n_q, d):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("G,n_q,tree", [(3, 43, False), (8, 20, True), (4, 64, True), (8, 32, False),
-                                        (16, 20, True), (8, 64, False), (257, 1, False), (5, 52, True)])
+                                        (16, 20, True), (8, 64, False), (257, 1, False), (5, 52, True),
+                                        (4, 11, True), (2, 16, False)])
 def test_pair_widths_ragged(G, n_q, tree, d):
     # 129..256 group rows run as one CTA whose two 128-row blocks take every
     # K/V tile; 257..512 as two such CTAs (320 and 512 rows here; 257 and 260
-    # leave the second CTA one or four rows, the rest of its warps idle);
-    # ragged prefixes include an empty history and a single key
+    # leave the second CTA one or four rows, the rest of its warps idle); up
+    # to 64 rows at d = 64 run as four consumer groups (44 rows, and 32 with
+    # every second warp idle); ragged prefixes include an empty history and a
+    # single key
     w = wl.Workload("t", B=3, Hq=2 * G, Hkv=2, d=d, n_q=n_q, prefix=2100, layers=1, V=10,
                     dtype="bf16", z_std=1, q_noise_std=1, q_noise_uses_T=True, tree=tree,
                     tree_nodes_max_depth=6, seed=60 + G + n_q)
