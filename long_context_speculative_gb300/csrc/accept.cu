@@ -646,7 +646,8 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     float* sw = reinterpret_cast<float*>(sel_dyn);   // [chunk] weights of this slice
     __shared__ int s_acc[kAcceptMaxNq], s_par[kAcceptMaxNq], s_kids[kAcceptMaxNq];
     __shared__ int s_key[2];
-    __shared__ int s_e, s_has_children;
+    __shared__ int s_e, s_has_children, s_depth, s_len;
+    __shared__ int s_nodes[kAcceptMaxNq];   // the winning path, leaf first
     __shared__ float s_seg[kSW];   // weight total of each warp's segment
     __shared__ float s_run[kSW][32], s_runi[kSW][32];   // lane runs of each segment: sums, inclusive prefix
     __shared__ float s_tot[2][kAcceptMaxCluster];   // every slice's total, per round
@@ -716,24 +717,22 @@ __global__ void __launch_bounds__(kST, 3) accept_select_kernel(const AcceptParam
     if (t == 0) {
         const int best = max(s_key[0], s_key[1]);
         const int best_len = best >> 8, best_leaf = 255 - (best & 255);
-        int nodes[kAcceptMaxNq];
         int depth = 0;
-        for (int v = best_leaf; v != 0; v = s_par[v]) nodes[depth++] = v;
-        const int e = best_len > 0 ? nodes[depth - best_len] : 0;
-        if (cs == 0) {
-            p.n_accepted[b] = best_len;
-            if (p.path) {
-                for (int k = 0; k < n_q; ++k)
-                    p.path[(int64_t)b * n_q + k] = k < best_len ? nodes[depth - 1 - k] : -1;
-            }
-            if (p.diag) {
-                for (int c = 0; c < 5; ++c) p.diag[(int64_t)b * n_q * 5 + c] = 0.f;
-            }
-        }
+        for (int v = best_leaf; v != 0; v = s_par[v]) s_nodes[depth++] = v;   // the leaf first
+        const int e = best_len > 0 ? s_nodes[depth - best_len] : 0;
+        s_depth = depth;
+        s_len = best_len;
         s_e = e;
         s_has_children = s_kids[e];
     }
     __syncthreads();
+    // the outputs (cluster rank 0), one path entry per thread
+    if (cs == 0 && t < n_q) {
+        const int len = s_len;
+        if (t == 0) p.n_accepted[b] = len;
+        if (p.path) p.path[(int64_t)b * n_q + t] = t < len ? s_nodes[s_depth - 1 - t] : -1;
+        if (p.diag && t < 5) p.diag[(int64_t)b * n_q * 5 + t] = 0.f;   // the root's row
+    }
 
     const int e = s_e;
     // the uniform of the draw, u_{e+1}: warp 0 needs it after the exchange
