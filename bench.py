@@ -429,27 +429,60 @@ def run_gpu(args, w):
     d2h = hO.numel() * hO.element_size() + hL.numel() * 4 + hres.numel() * 4
     res_dev = torch.empty(2 * w.B, dtype=torch.int32, device=dev)
 
-    def e2e_step(seed):
-        dQ.copy_(hQ, non_blocking=True)
-        z.copy_(hz, non_blocking=True); q.copy_(hq, non_blocking=True)
-        tok.copy_(htok, non_blocking=True)
+    # The copies run on two copy streams beside the compute stream, within each
+    # step: the step's inputs go up once the previous step's kernels are done
+    # with the buffers (Q first, which the first layer waits for; z, q and the
+    # tokens meanwhile, which only the acceptance waits for), and O and LSE of
+    # every layer come back while the acceptance runs.  Nothing is enqueued
+    # on the compute stream between two layers, so consecutive launches keep
+    # their programmatic overlap.
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+    ev_q = torch.cuda.Event()
+    ev_zq = torch.cuda.Event()
+    ev_attn = torch.cuda.Event()
+    ev_res = torch.cuda.Event()
+    ev_back = torch.cuda.Event()
+
+    def e2e_step(seed, first):
+        up.wait_stream(stream)   # the previous step's kernels are done with dQ, z, q, tok
+        with torch.cuda.stream(up):
+            dQ.copy_(hQ, non_blocking=True)
+            ev_q.record(up)
+            z.copy_(hz, non_blocking=True); q.copy_(hq, non_blocking=True)
+            tok.copy_(htok, non_blocking=True)
+            ev_zq.record(up)
+        stream.wait_event(ev_q)
+        if not first:
+            stream.wait_event(ev_back)   # the previous step's results are out
         for layer in range(w.layers):
             rapid.rapid_verify_attn(dQ[layer], Ks[layer], Vs[layer], prefix_len, mask, 0.0,
                                     Os[layer], Ls[layer], ws_attn)
+        ev_attn.record(stream)
+        stream.wait_event(ev_zq)
         rapid.rapid_accept(z, q, tok, par, w.T, w.eta, seed, rapid.RAPID_ACCEPT_TAIL_CLAMP,
                            res_dev[:w.B], res_dev[w.B:], None, None, ws_acc)
-        hO.copy_(O_all, non_blocking=True)
-        hL.copy_(L_all, non_blocking=True)
-        hres.copy_(res_dev, non_blocking=True)
+        ev_res.record(stream)
+        down.wait_event(ev_attn)
+        with torch.cuda.stream(down):
+            hO.copy_(O_all, non_blocking=True)
+            hL.copy_(L_all, non_blocking=True)
+        down.wait_event(ev_res)
+        with torch.cuda.stream(down):
+            hres.copy_(res_dev, non_blocking=True)
+            ev_back.record(down)   # every result of this step is on the host
 
     for i in range(args.warmup):
-        e2e_step(i)
+        e2e_step(i, i == 0)
     torch.cuda.synchronize()
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
+    up.wait_event(e_start)
+    down.wait_event(e_start)
     for s in range(args.steps):
-        e2e_step(0x5EED0000 + s)
+        e2e_step(0x5EED0000 + s, False)
+    stream.wait_event(ev_back)   # the last step's results are on the host
     e_end.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e_start.elapsed_time(e_end), dev)
