@@ -15,19 +15,22 @@
 //              they are its two 128-row blocks and both take every tile);
 //              warp w owns TMEM lane quadrant w % 4, i.e. rows 32 (w % 4) ..
 //              + 31 of its group's M = 128 operand.  A
-//              group turns its S tile into P (bf16, its own shared buffer),
-//              keeps its running max / sum and rescales its O in TMEM when the
-//              max grows by more than 2^8.  At the end the two groups combine
-//              their (O, m, l) into the split's one partial.
-//   warp 8     TMA producer: 64-key K and V tiles into a 6-stage ring (5 when
-//              the group has more than 64 query rows); the
-//              last split also loads the n_q speculative rows as one more
-//              tile, which the softmax masks with the chain / tree mask.
+//              group turns its S tile into P (bf16, its own shared buffer;
+//              two per block in a 256-row CTA), keeps its running max / sum
+//              and rescales its O in TMEM when the max grows by more than 2^8.
+//              At the end the two groups combine their (O, m, l) into the
+//              split's one partial (a 256-row CTA's blocks write their own).
+//   warp 8     TMA producer: 64-key K and V tiles into a ring of 32 KB (16 KB
+//              at d = 64) stages filling the shared memory left; the last
+//              split also loads the n_q speculative rows as one more tile,
+//              which the softmax masks with the chain / tree mask.
 //   warp 11    allocates TMEM and issues the MMAs (one thread), in the order
 //              their inputs become ready: S_j = Q K_j^T (M128 N64 K = d, two S
 //              buffers per group, so S runs a tile ahead of the softmax; in a
-//              256-row CTA one per block, released as soon as it is loaded)
-//              and O_g += P_i V_i (M128 N = d K64).
+//              256-row CTA one per block, released as soon as it is loaded,
+//              with Q in TMEM) and O_g += P_i V_i (M128 N = d K64).  It sits
+//              on sub-partition 3, whose softmax warps are the most often
+//              idle: issue slots taken there slow the tensor pipe's intake.
 // Shared-memory operands use the 128-byte swizzle; Q, K and P are K-major,
 // V is MN-major (d contiguous).  Every mbarrier wait is bounded in wall-clock
 // time; on a timeout the kernel records an error code, stops issuing work,
