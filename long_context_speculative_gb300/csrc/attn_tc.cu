@@ -209,6 +209,14 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     const int r0 = rb * L::kCtaRows;               // first group row of this CTA
     const int Rb = min(L::kCtaRows, p.R - r0);     // rows of this CTA
     const int g = blockIdx.y;
+    // The lane quadrants of consumer group gr that hold rows of this CTA: their
+    // softmax warps take part, the others leave at once (a group without rows
+    // keeps one warp, which runs the barrier protocol alone).
+    auto live_quadrants = [&](int gr) -> int {
+        const int rows = L::kRowGroups ? Rb - 128 * gr : Rb;
+        const int q = (rows + 31) / 32;
+        return q < 1 ? 1 : (q > L::kActiveQuadrants ? L::kActiveQuadrants : q);
+    };
     // Input-free set-up first: it may overlap the previous kernel in the stream.
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -216,9 +224,10 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mbar_init(&bars->kv_empty[i], 1);
         }
         for (int u = 0; u < 4; ++u) mbar_init(&bars->s_full[u], 1);
-        for (int gr = 0; gr < 2; ++gr) mbar_init(&bars->s_free[gr], L::kActiveQuadrants);
+        for (int gr = 0; gr < 2; ++gr) mbar_init(&bars->s_free[gr], live_quadrants(gr));
         for (int u = 0; u < 4; ++u) {
-            mbar_init(&bars->p_full[u], L::kGroupThreads);
+            // p_full[2 g + u] of block g in a 256-row CTA, p_full[g] otherwise
+            mbar_init(&bars->p_full[u], 32 * live_quadrants(L::kRowGroups ? (u >> 1) : (u & 1)));
             mbar_init(&bars->p_free[u], 1);
         }
         mbar_init(&bars->drain, 1);
@@ -550,7 +559,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             mma_commit(&bars->drain);
             mbar_wait_sleep(&bars->drain, 0, p.err, kRoleMma | kBarDrain);
         }
-    } else if (warp < kSoftmaxWarps && (warp & 3) < L::kActiveQuadrants) {
+    } else if (warp < kSoftmaxWarps && (warp & 3) < live_quadrants(warp >> 2)) {
         // ------------------------------ softmax warps -------------------------
         // Group gr = warp / 4 takes tiles gr, gr + 2, ... (with ROWS = 256:
         // every tile, for row block gr); warp w owns TMEM lane quadrant w % 4,
@@ -789,7 +798,7 @@ attn_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmK,
             pub[128 + r] = k_local > 0 ? l_run : 0.f;
         }
         if (!ok && lane == 0) bars->grp_ok[gr] = 0;   // any warp of the group can veto
-        asm volatile("bar.sync 1, %0;" ::"n"(2 * L::kGroupThreads) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"r"(2 * 32 * live_quadrants(0)) : "memory");
         ok = bars->grp_ok[0] && bars->grp_ok[1];
         if (ok) {
             tc_fence_after();
